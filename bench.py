@@ -1,0 +1,470 @@
+"""Benchmark one decode step (append + paged decode attention) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl native|reference]
+
+A step is one layer's decode step over one batch: pkv_kv_append of each
+sequence's newest K/V row, then pkv_paged_decode_attention over all cached
+tokens.  Inputs are seeded synthetic tensors of the workload's shapes,
+resident in HBM before the timed region.  The timed region is K steps
+captured in one CUDA graph, bracketed by a barrier and a synchronize, timed
+with CUDA events on the launching stream.  L2 hygiene: the steps rotate over
+enough copies of the cache pool that each step reads pages no other step
+touched within the last (R-1) steps (total footprint >= 4x the 129 MB L2).
+
+Printed (rank 0, one JSON line): value = algorithmic bytes per step / step
+time in GB/s; tokens/s per layer; the dominant kernel's roofline against the
+measured HBM copy bandwidth; an end-to-end figure through the same C ABI with
+the step's inputs copied from pinned host memory and the output read back
+inside the timed region; the CPU oracle timed on a bounded sample; SM clocks
+sampled during the timed region.
+
+Multi-GPU: the decode path has no exchange step, so N ranks run N independent
+replicas of the workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import paged_kv_cache_250_gb300 as pkv  # noqa: E402
+from paged_kv_cache_250_gb300 import workloads as wl  # noqa: E402
+
+DEFAULT_CONFIG = "llama3_8b_b32_ctx1-4096_bf16"
+METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and tokens/s per layer"
+L2_BYTES = 129 * 1024 * 1024
+PEAK_FALLBACK_GBS = 6800.0
+_CODE = {"f16": pkv.PKV_F16, "bf16": pkv.PKV_BF16, "e4m3": pkv.PKV_FP8_E4M3}
+_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [l for (t, l) in self.lines if t0 - 0.05 <= t <= t1 + 0.05] or \
+            [l for (_, l) in self.lines]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(cfg, ctx: torch.Tensor):
+    """Bytes the step must move (read or write) at minimum.
+
+    attention: every cached K and V element once, q, the output, the block-
+    table entries used and the context lengths (+ the FP8 scales);
+    append: the new K/V rows read and written, and the slot mapping."""
+    B, Hq, Hkv, d = cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim
+    e_c = cfg.cache_elem_bytes
+    e_q = 2
+    e_out = 2
+    ctx64 = ctx.to(torch.int64)
+    pages = int(((ctx64 + wl.PAGE - 1) // wl.PAGE).sum())
+    attn = int(ctx64.sum()) * Hkv * d * 2 * e_c + B * Hq * d * (e_q + e_out) + pages * 4 + 4 * B
+    if cfg.cache == "e4m3":
+        attn += 8 * Hkv
+    append = B * Hkv * d * 2 * (2 + e_c) + 8 * B
+    return attn, append
+
+
+# ---------------------------------------------------------------- native arm
+class Step:
+    """Device state of one workload: R pool replicas, inputs, outputs."""
+
+    def __init__(self, cfg, device, replicas: int, hint: int):
+        self.cfg = cfg
+        self.dev = device
+        w = wl.generate(cfg, device=device)
+        self.w = w
+        self.hint = hint
+        self.q = w.q.contiguous()
+        self.k_new = w.k_new.contiguous()
+        self.v_new = w.v_new.contiguous()
+        self.slot = w.slot_mapping.to(device)
+        self.tables = w.block_tables.to(device)
+        self.ctx = w.ctx.to(device)
+        self.k_scale = None if w.k_scale is None else w.k_scale.float().contiguous()
+        self.v_scale = None if w.v_scale is None else w.v_scale.float().contiguous()
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.kc = [w.k_cache] + [w.k_cache.clone() for _ in range(replicas - 1)]
+        self.vc = [w.v_cache] + [w.v_cache.clone() for _ in range(replicas - 1)]
+        self.desc = pkv.make_desc(w.num_blocks, wl.PAGE, cfg.kv_heads, cfg.q_heads,
+                                  cfg.head_dim, _CODE[cfg.cache], self.k_scale, self.v_scale,
+                                  self.err)
+        n = pkv.pkv_decode_workspace_bytes(self.desc, cfg.batch, w.max_blocks_per_seq, hint)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=device)
+        self.out = torch.empty(cfg.batch, cfg.q_heads, cfg.head_dim, dtype=torch.bfloat16
+                               if cfg.cache != "f16" else torch.float16, device=device)
+        # the K/V inputs of the per-head K/V projections are what drives the bytes
+        self.R = replicas
+
+    def append(self, r, stream):
+        pkv.pkv_kv_append(self.desc, self.kc[r], self.vc[r], self.slot, self.k_new, self.v_new,
+                          stream=stream)
+
+    def decode(self, r, stream):
+        pkv.pkv_paged_decode_attention(self.desc, self.q, self.kc[r], self.vc[r], self.tables,
+                                       self.ctx, self.cfg.softmax_scale, self.out, self.ws,
+                                       self.hint, stream=stream)
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def run_native(args, cfg, rank, world, device):
+    stream = torch.cuda.Stream(device)
+    per_set = wl.cache_bytes_per_step(cfg, torch.tensor([0]))  # placeholder
+    hint = {"llama3_8b_b32_ctx1-4096_bf16": 4096}.get(cfg.name, 0)
+    # replicas: enough pool copies that the rotation spans >= 4x L2
+    w_probe_bytes = None
+    with torch.cuda.stream(stream):
+        probe = Step(cfg, device, 1, hint)
+    pool_bytes = probe.kc[0].numel() * probe.kc[0].element_size() * 2
+    R = max(1, min(8, -(-4 * L2_BYTES // pool_bytes)))
+    del probe
+    torch.cuda.empty_cache()
+    with torch.cuda.stream(stream):
+        st = Step(cfg, device, R, hint)
+    torch.cuda.synchronize(device)
+    attn_bytes, append_bytes = algorithmic_bytes(cfg, st.w.ctx)
+    step_bytes = attn_bytes + append_bytes
+    K, W = args.steps, args.warmup
+
+    # warm-up (also sets kernel attributes before capture)
+    for i in range(W):
+        st.append(i % R, stream)
+        st.decode(i % R, stream)
+    stream.synchronize()
+
+    # graph of K steps, events between the two calls of each step
+    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+          for _ in range(K)]
+
+    def body_events():
+        for i in range(K):
+            ev[i][0].record(stream)
+            st.append(i % R, stream)
+            ev[i][1].record(stream)
+            st.decode(i % R, stream)
+            ev[i][2].record(stream)
+
+    def body_plain():
+        for i in range(K):
+            st.append(i % R, stream)
+            st.decode(i % R, stream)
+
+    g_plain = capture(body_plain, stream)
+    g_events = capture(body_events, stream)
+
+    # e2e: pinned host inputs copied in, output copied out, every step
+    h_q = st.q.cpu().pin_memory()
+    h_k = st.k_new.cpu().pin_memory()
+    h_v = st.v_new.cpu().pin_memory()
+    h_slot = st.slot.cpu().pin_memory()
+    h_tab = st.tables.cpu().pin_memory()
+    h_ctx = st.ctx.cpu().pin_memory()
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slot, h_tab, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def body_e2e():
+        for i in range(K):
+            st.q.copy_(h_q, non_blocking=True)
+            st.k_new.copy_(h_k, non_blocking=True)
+            st.v_new.copy_(h_v, non_blocking=True)
+            st.slot.copy_(h_slot, non_blocking=True)
+            st.tables.copy_(h_tab, non_blocking=True)
+            st.ctx.copy_(h_ctx, non_blocking=True)
+            st.append(i % R, stream)
+            st.decode(i % R, stream)
+            h_out.copy_(st.out, non_blocking=True)
+
+    g_e2e = capture(body_e2e, stream)
+    torch.cuda.synchronize(device)
+
+    def timed(graph):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    g_plain.replay()  # graph warm-up
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    ms_total = timed(g_plain)
+    t1 = time.time()
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    ms_events = timed(g_events)
+    ms_e2e = timed(g_e2e)
+    err = int(st.err.item())
+    if err != 0:
+        raise RuntimeError(f"device error word {err} ({pkv.pkv_status_string(err)})")
+
+    append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    decode_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    ms_step = ms_total / K
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = attn_bytes / (decode_ms * 1e-3) / 1e9
+    traffic = committed_traffic(cfg.name)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[cfg.cache],
+        "data": "synthetic (seeded N(0,1) q/k/v, uniform ragged context lengths, "
+                "permuted block tables)",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
+                   "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "page_size": wl.PAGE,
+                   "cache_dtype": cfg.cache, "total_context_tokens": int(st.w.ctx.sum()),
+                   "l2": f"rotating {R} cache-pool copies ({R * pool_bytes / 1e6:.0f} MB, "
+                         f">= 4x L2); every step reads cold pages",
+                   "timing": "K steps in one CUDA graph, CUDA events on the launch stream",
+                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "percent_of_peak": round(100 * value / world / peak, 1),
+        "tokens_per_s_per_layer": round(world * cfg.batch / (ms_step * 1e-3), 1),
+        "breakdown_us": {"append": round(append_ms * 1e3, 2),
+                         "decode_attention": round(decode_ms * 1e3, 2),
+                         "step_with_events": round(ms_events / K * 1e3, 2)},
+        "bytes_per_step": {"attention": attn_bytes, "append": append_bytes},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "kernel": "pkv_paged_decode_attention "
+                     "(decode_split_kernel + combine_kernel)", "peak_kind": peak_kind},
+        "e2e": {"value": round(world * step_bytes / (ms_e2e / K * 1e-3) / 1e9, 1),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e / K, 5)},
+        "gpu_launches": K * 3,
+        "clocks": clocks,
+    }
+    return res, st
+
+
+def committed_traffic(workload):
+    """DRAM traffic per decode launch from the committed ncu summary, if the
+    kernel sources still hash to what was profiled; else null."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+    except Exception:
+        return None
+    ent = j.get(workload)
+    if not ent or ent.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_250_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_sample(cfg, w, max_seconds):
+    """Time the CPU oracle on whole sequences of the workload (all query
+    heads), taking sequences in order until about `max_seconds` of work."""
+    import numpy as np
+
+    import oracle
+    threads = oracle.max_threads()
+    g = cfg.group
+    done_bytes = 0
+    t_spent = 0.0
+    seqs = 0
+    for b in range(cfg.batch):
+        n = int(w.ctx[b])
+        if n == 0:
+            continue
+        Kb = w.K_log[b, :n].double().cpu().numpy()[None]
+        Vb = w.V_log[b, :n].double().cpu().numpy()[None]
+        qb = w.q[b].double().cpu().numpy()[None]
+        t0 = time.perf_counter()
+        oracle.decode_attention(qb, Kb, Vb, np.array([n], np.int32), cfg.softmax_scale,
+                                nthreads=threads)
+        t_spent += time.perf_counter() - t0
+        done_bytes += n * cfg.kv_heads * cfg.head_dim * 2 * cfg.cache_elem_bytes
+        seqs += 1
+        if t_spent >= max_seconds:
+            break
+    return done_bytes, t_spent, seqs, threads
+
+
+def cpu_baseline(cfg, w, max_seconds=10.0):
+    b, t, seqs, threads = oracle_sample(cfg, w, max_seconds)
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{seqs} of {cfg.batch} sequences, all {cfg.q_heads} query heads, "
+                      f"fp64 C oracle with OpenMP; {b / 1e6:.1f} MB of cache in {t:.2f} s"}
+
+
+def run_reference(args, cfg):
+    import numpy as np  # noqa: F401
+    w = wl.generate(cfg, device="cpu")
+    K, W = args.steps, args.warmup
+    budget = max(0.2, 120.0 / max(1, K + W))  # whole run within a few minutes
+    for _ in range(W):
+        oracle_sample(cfg, w, budget)
+    vals, times = [], []
+    total_b, total_t = 0, 0.0
+    for _ in range(K):
+        b, t, seqs, threads = oracle_sample(cfg, w, budget)
+        total_b += b
+        total_t += t
+        times.append(t)
+    value = total_b / total_t / 1e9
+    cb = {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+          "sample": f"per step the first {seqs} sequence(s) of {cfg.name} (all query heads), "
+                    f"fp64 C oracle, OpenMP"}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(1e3 * total_t / K, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg.name},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = wl.CONFIGS[args.config]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for the native arm")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    pkv.load_library()
+    res, st = run_native(args, cfg, rank, world, device)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            wcpu = wl.generate(cfg, device="cpu")
+            res["cpu_baseline"] = cpu_baseline(cfg, wcpu)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * pkv.h -- C ABI of the paged-KV decode-attention library (libpkv.so).
+ *
+ * One decode step for one attention layer is two calls on the caller's CUDA
+ * stream:
+ *
+ *   1. pkv_kv_append: write the new token's K and V rows into the cache
+ *      pages named by a slot mapping.
+ *   2. pkv_paged_decode_attention: for every sequence and query head, one
+ *      (1,N) attention row over the cached keys and values, read through the
+ *      sequence's block table.
+ *
+ * Sources (web pages):
+ *   [KVFA] "KV Cache & Flash Attention." (kvcache-7e2.pages.dev)
+ *   [DF]   "KV Cache & FlashAttention" (deepforge.srivtx.xyz)
+ *   [AP]   "KV cache, paged, flash and sparse attention" (abhishekpatel.co)
+ *
+ * Conventions shared by every entry point
+ *   - All buffers are owned by the caller.  The library allocates and frees
+ *     nothing and keeps no state beyond a per-device cache of the SM count.
+ *   - Pointers are DEVICE pointers unless the comment says host.  The
+ *     descriptor itself is a host struct.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  They return once the kernels are enqueued and never
+ *     synchronise.
+ *   - Argument errors are reported before any launch.  Launch failures
+ *     return PKV_ERR_CUDA.  Data-dependent errors found on the device (a slot
+ *     or block-table entry outside the pool, a context longer than the table)
+ *     skip the offending work and are recorded in the optional device word
+ *     `err_word` (first error wins; the library never clears it).  No kernel
+ *     traps.
+ *   - Cache layout ("HND"): k_cache and v_cache are [num_blocks][num_kv_heads]
+ *     [page_size][head_dim] elements of `cache_dtype`, so one (block, KV head)
+ *     page is a contiguous run of page_size * head_dim elements.  The base
+ *     address must be 16-byte aligned.
+ *   - Query head hq reads KV head hq / (num_q_heads / num_kv_heads).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, ...    */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, group, dtype  */
+  PKV_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
+  PKV_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed          */
+  PKV_ERR_BOUNDS = 5,      /* device: slot / block id / context out of range */
+  PKV_ERR_TIMEOUT = 6      /* device: a bounded wait gave up                */
+} pkv_status;
+
+typedef enum {
+  PKV_F16 = 0,
+  PKV_BF16 = 1,
+  PKV_FP8_E4M3 = 2, /* OCP E4M3 (bias 7, max 448, no infinities)         */
+  PKV_F32 = 3
+} pkv_dtype;
+
+/* Shape of the paged cache, shared by both calls.
+ * Supported: page_size 16; head_dim 64 or 128 (128 for FP8_E4M3);
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; cache_dtype F16, BF16 or
+ * FP8_E4M3; num_blocks * num_kv_heads * page_size < 2^31. */
+typedef struct {
+  uint32_t struct_size;  /* sizeof(pkv_cache_desc); checked               */
+  int32_t num_blocks;    /* physical blocks in the pool (NB)               */
+  int32_t page_size;     /* tokens per block (P)                           */
+  int32_t num_kv_heads;  /* Hkv                                            */
+  int32_t num_q_heads;   /* Hq, a multiple of Hkv                          */
+  int32_t head_dim;      /* d                                              */
+  pkv_dtype cache_dtype; /* F16 | BF16 | FP8_E4M3                          */
+  const float* k_scale;  /* device fp32 [Hkv]; FP8 only: stored K = k/scale */
+  const float* v_scale;  /* device fp32 [Hkv]; FP8 only                     */
+  int32_t* err_word;     /* optional device int32; NULL = do not report    */
+} pkv_cache_desc;
+
+/* Append (scatter) new K/V rows into their cache slots.
+ * [KVFA] KV-cache section (append one K and one V per token) and
+ * PagedAttention section (position -> (block, offset)); [AP] "Following one
+ * new token through the cache".
+ *   slot_mapping int64 [num_tokens]: slot = block * page_size + offset; a
+ *                negative slot skips the token; a slot >= num_blocks *
+ *                page_size is a device-detected PKV_ERR_BOUNDS.
+ *   k, v         [num_tokens][num_kv_heads][head_dim] of kv_dtype (F16 or
+ *                BF16; for 16-bit caches it must equal cache_dtype).
+ *   For FP8_E4M3 caches each element is divided by its head's scale in IEEE
+ *   fp32 and encoded round-to-nearest-even with saturation to +-448.
+ *   Slots written by two tokens of one call race; the caller avoids it. */
+PKV_API pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache,
+                         void* v_cache, const int64_t* slot_mapping,
+                         const void* k, const void* v, int32_t num_tokens,
+                         pkv_dtype kv_dtype, pkv_stream_t stream);
+
+/* Bytes of device workspace pkv_paged_decode_attention needs for these
+ * sizes on the current device (it depends on the SM count).  Returns 0 on
+ * invalid arguments.  The workspace holds the split partials and a per-
+ * (sequence, KV head) split count; its contents need no initialisation. */
+PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                  int32_t max_blocks_per_seq,
+                                  int32_t max_context_len_hint);
+
+/* Decode attention for one layer.
+ * [KVFA] KV-cache section ((1,N) row per step), Flash Attention and
+ * online-softmax sections (running max and sum, rescale by exp(m_old -
+ * m_new)), PagedAttention section (the kernel takes the page table and
+ * gathers K and V); [DF] running-summary paragraph.
+ *   q             [batch][num_q_heads][head_dim] of q_dtype (F16 | BF16;
+ *                 for 16-bit caches equal to cache_dtype).  With an FP8
+ *                 cache q is used in fp16 and must lie within +-65504.
+ *   block_tables  int32 [batch][max_blocks_per_seq]; entry p of row b is the
+ *                 block holding tokens p*P .. p*P+P-1 of sequence b.  Rows
+ *                 may share blocks (prefix sharing); entries past a
+ *                 sequence's last page are never read.
+ *   context_lens  int32 [batch]; tokens attended, including one appended by
+ *                 a preceding pkv_kv_append on the same stream.  0 gives a
+ *                 zero output row; > max_blocks_per_seq * P is a device-
+ *                 detected PKV_ERR_BOUNDS (that sequence's output is zero).
+ *   max_context_len_hint  0, or an upper bound on context_lens used only to
+ *                 size the launch; the kernel reads the true lengths.
+ *   scale         softmax scale applied to q.k (usually 1/sqrt(head_dim)).
+ *   out           [batch][num_q_heads][head_dim] of out_dtype (F16 | BF16 |
+ *                 F32), rounded to nearest even.  Must not alias inputs.
+ *   workspace     device buffer of at least pkv_decode_workspace_bytes(),
+ *                 256-byte aligned; not shared with concurrent calls.  */
+PKV_API pkv_status pkv_paged_decode_attention(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
+    int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
+    pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
+    pkv_stream_t stream);
+
+/* Cache bytes per token across all layers: 2 * layers * kv_heads * head_dim
+ * * elem_bytes ([AP] "Opening the hood: how big is the notebook?"; [DF]
+ * cache-size paragraph).  Host-only. */
+PKV_API uint64_t pkv_kv_bytes_per_token(int32_t layers, int32_t kv_heads,
+                                int32_t head_dim, int32_t elem_bytes);
+
+/* Static, human-readable name of a status code.  Host-only. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH.  Host-only. */
+PKV_API int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,222 @@
+"""Python binding of libpkv.so: paged-KV single-token decode attention for GB300.
+
+Argument marshalling only.  Every step of the decode path runs in the CUDA
+kernels behind the C ABI declared in ``include/pkv.h``; torch supplies device
+memory and streams.  The functions carry the C names:
+
+    pkv_kv_append                 write new K/V rows into their cache slots
+    pkv_decode_workspace_bytes    workspace size for a decode call
+    pkv_paged_decode_attention    one (1,N) attention row per query head
+    pkv_kv_bytes_per_token        cache bytes per token (host helper)
+    pkv_status_string, pkv_version
+
+If the library is missing it is built on first use with nvcc; if that is not
+possible every call raises.  There is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "PkvError", "CacheDesc", "make_desc", "load_library", "library_path",
+    "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
+    "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
+    "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
+    "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
+    "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "EXPORTED_SYMBOLS",
+]
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE = 0, 1, 2, 3
+PKV_ERR_CUDA, PKV_ERR_BOUNDS, PKV_ERR_TIMEOUT = 4, 5, 6
+PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
+
+EXPORTED_SYMBOLS = (
+    "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
+    "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
+)
+
+_DTYPE_CODE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16,
+               torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPE_CODE[torch.float8_e4m3fn] = PKV_FP8_E4M3
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {pkv_status_string(status)}")
+
+
+class CacheDesc(ctypes.Structure):
+    """Mirror of ``pkv_cache_desc`` (include/pkv.h)."""
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("num_blocks", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("cache_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
+        ("err_word", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libpkv.so (building it with nvcc if absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P, I32, U64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
+        D = ctypes.POINTER(CacheDesc)
+        lib.pkv_kv_append.restype = I32
+        lib.pkv_kv_append.argtypes = [D, P, P, P, P, P, I32, I32, P]
+        lib.pkv_decode_workspace_bytes.restype = SZ
+        lib.pkv_decode_workspace_bytes.argtypes = [D, I32, I32, I32]
+        lib.pkv_paged_decode_attention.restype = I32
+        lib.pkv_paged_decode_attention.argtypes = [D, P, P, P, P, P, I32, I32, I32,
+                                                   ctypes.c_float, P, I32, I32, P, SZ, P]
+        lib.pkv_kv_bytes_per_token.restype = U64
+        lib.pkv_kv_bytes_per_token.argtypes = [I32, I32, I32, I32]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_status_string.argtypes = [I32]
+        lib.pkv_version.restype = I32
+        lib.pkv_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev_ptr(t: Optional[torch.Tensor], name: str):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(num_blocks: int, page_size: int, num_kv_heads: int, num_q_heads: int,
+              head_dim: int, cache_dtype: int, k_scale: Optional[torch.Tensor] = None,
+              v_scale: Optional[torch.Tensor] = None,
+              err_word: Optional[torch.Tensor] = None) -> CacheDesc:
+    """Build a ``pkv_cache_desc``.  Tensors passed here must outlive its use."""
+    d = CacheDesc()
+    d.struct_size = ctypes.sizeof(CacheDesc)
+    d.num_blocks = num_blocks
+    d.page_size = page_size
+    d.num_kv_heads = num_kv_heads
+    d.num_q_heads = num_q_heads
+    d.head_dim = head_dim
+    d.cache_dtype = cache_dtype
+    d.k_scale = k_scale.data_ptr() if k_scale is not None else None
+    d.v_scale = v_scale.data_ptr() if v_scale is not None else None
+    d.err_word = err_word.data_ptr() if err_word is not None else None
+    return d
+
+
+def _check(status: int, where: str):
+    if status != PKV_OK:
+        raise PkvError(status, where)
+
+
+def pkv_kv_append(desc: CacheDesc, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  slot_mapping: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  stream=None) -> None:
+    """k, v: [T][Hkv][d] (fp16/bf16); slot_mapping: int64 [T]."""
+    lib = load_library()
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if k.dtype != v.dtype or k.shape != v.shape:
+        raise ValueError("k and v must match")
+    st = lib.pkv_kv_append(ctypes.byref(desc), _dev_ptr(k_cache, "k_cache"),
+                           _dev_ptr(v_cache, "v_cache"), _dev_ptr(slot_mapping, "slot_mapping"),
+                           _dev_ptr(k, "k"), _dev_ptr(v, "v"), int(k.shape[0]),
+                           _DTYPE_CODE.get(k.dtype, -1), _stream_handle(stream, k.device))
+    _check(st, "pkv_kv_append")
+
+
+def pkv_decode_workspace_bytes(desc: CacheDesc, batch: int, max_blocks_per_seq: int,
+                               max_context_len_hint: int = 0) -> int:
+    lib = load_library()
+    return int(lib.pkv_decode_workspace_bytes(ctypes.byref(desc), int(batch),
+                                              int(max_blocks_per_seq),
+                                              int(max_context_len_hint)))
+
+
+def pkv_paged_decode_attention(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
+                               v_cache: torch.Tensor, block_tables: torch.Tensor,
+                               context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                               workspace: torch.Tensor, max_context_len_hint: int = 0,
+                               stream=None) -> None:
+    """q/out: [B][Hq][d]; block_tables int32 [B][MBS]; context_lens int32 [B]."""
+    lib = load_library()
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    B, mbs = int(block_tables.shape[0]), int(block_tables.shape[1])
+    st = lib.pkv_paged_decode_attention(
+        ctypes.byref(desc), _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(context_lens, "context_lens"), B, mbs, int(max_context_len_hint),
+        float(scale), _dev_ptr(out, "out"), _DTYPE_CODE.get(q.dtype, -1),
+        _DTYPE_CODE.get(out.dtype, -1), _dev_ptr(workspace, "workspace"),
+        int(workspace.numel() * workspace.element_size()), _stream_handle(stream, q.device))
+    _check(st, "pkv_paged_decode_attention")
+
+
+def pkv_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    return int(load_library().pkv_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes))
+
+
+def pkv_status_string(status: int) -> str:
+    return load_library().pkv_status_string(int(status)).decode()
+
+
+def pkv_version() -> int:
+    return int(load_library().pkv_version())
+
+
+@dataclass
+class DecodeBuffers:
+    """Workspace sized for a launch shape (convenience for callers)."""
+    workspace: torch.Tensor
+
+    @staticmethod
+    def allocate(desc: CacheDesc, batch: int, max_blocks_per_seq: int,
+                 max_context_len_hint: int = 0, device="cuda") -> "DecodeBuffers":
+        n = pkv_decode_workspace_bytes(desc, batch, max_blocks_per_seq, max_context_len_hint)
+        if n == 0:
+            raise PkvError(PKV_ERR_INVALID_ARG, "pkv_decode_workspace_bytes")
+        return DecodeBuffers(torch.empty(n, dtype=torch.uint8, device=device))

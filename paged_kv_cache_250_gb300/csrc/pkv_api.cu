@@ -1,0 +1,271 @@
+// pkv_api.cu -- the C ABI (include/pkv.h): argument validation, launch
+// sizing, tensor-map encoding and kernel dispatch.  No allocation, no
+// synchronisation, no state beyond a per-device SM-count cache.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+using pkv::kPageSize;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < kMaxDevices) {
+    int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return -1;
+  if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by both calls.
+pkv_status check_desc(const pkv_cache_desc* d) {
+  if (d == nullptr || d->struct_size != sizeof(pkv_cache_desc)) return PKV_ERR_INVALID_ARG;
+  if (d->num_blocks <= 0 || d->page_size <= 0 || d->num_kv_heads <= 0 ||
+      d->num_q_heads <= 0 || d->head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (d->num_q_heads % d->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (d->page_size != kPageSize) return PKV_ERR_UNSUPPORTED;
+  const int g = d->num_q_heads / d->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PKV_ERR_UNSUPPORTED;
+  switch (d->cache_dtype) {
+    case PKV_F16:
+    case PKV_BF16:
+      if (d->head_dim != 64 && d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+      break;
+    case PKV_FP8_E4M3:
+      if (d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+      if (d->k_scale == nullptr || d->v_scale == nullptr) return PKV_ERR_INVALID_ARG;
+      break;
+    default:
+      return PKV_ERR_UNSUPPORTED;
+  }
+  const int64_t rows = (int64_t)d->num_blocks * d->num_kv_heads * d->page_size;
+  if (rows >= (int64_t)1 << 31) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+pkv::CacheKind kind_of(pkv_dtype t) {
+  return t == PKV_FP8_E4M3 ? pkv::kCacheE4M3 : (t == PKV_BF16 ? pkv::kCacheBF16 : pkv::kCacheF16);
+}
+
+struct WsLayout {
+  size_t ml_off, o_off, seg_off, total;
+  int ctas;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t hint,
+                   int num_sms) {
+  const int64_t g = d->num_q_heads / d->num_kv_heads;
+  const int64_t cap = (int64_t)mbs * kPageSize;
+  const int64_t len = (hint > 0 && hint < cap) ? hint : cap;
+  const int64_t pages_bound = (int64_t)batch * d->num_kv_heads * ((len + kPageSize - 1) / kPageSize);
+  // at least two pages per warp; at most kDecodeCtasPerSm CTAs per SM
+  int64_t ctas = (pages_bound + 2 * pkv::kDecodeWarps - 1) / (2 * pkv::kDecodeWarps);
+  const int64_t max_ctas = (int64_t)num_sms * pkv::kDecodeCtasPerSm;
+  if (ctas > max_ctas) ctas = max_ctas;
+  if (ctas < 1) ctas = 1;
+  const int64_t chunks = ctas * pkv::kDecodeWarps + (int64_t)batch * d->num_kv_heads;
+  WsLayout w;
+  w.ctas = (int)ctas;
+  w.ml_off = 0;
+  w.o_off = align256(w.ml_off + (size_t)chunks * g * 2 * sizeof(float));
+  w.seg_off = align256(w.o_off + (size_t)chunks * g * d->head_dim * sizeof(float));
+  w.total = align256(w.seg_off + (size_t)batch * d->num_kv_heads * 2 * sizeof(int32_t));
+  return w;
+}
+
+pkv_status encode_cache_map(CUtensorMap* map, const void* cache, const pkv_cache_desc* d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return PKV_ERR_CUDA;
+  const bool fp8 = d->cache_dtype == PKV_FP8_E4M3;
+  const cuuint64_t elem = fp8 ? 1 : 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim,
+                              (cuuint64_t)d->num_blocks * d->num_kv_heads * d->page_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * elem};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)d->page_size};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                  const_cast<void*>(cache), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, const void* k, const void* v,
+                         int32_t num_tokens, pkv_dtype kv_dtype, pkv_stream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !slot_mapping || !k || !v) return PKV_ERR_INVALID_ARG;
+  if (kv_dtype != PKV_F16 && kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (desc->cache_dtype != PKV_FP8_E4M3 && kv_dtype != desc->cache_dtype)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(slot_mapping, 8))
+    return PKV_ERR_INVALID_ARG;
+  pkv::AppendParams a;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.slot_mapping = slot_mapping;
+  a.k = k;
+  a.v = v;
+  a.k_scale = desc->k_scale;
+  a.v_scale = desc->v_scale;
+  a.err_word = desc->err_word;
+  a.T = num_tokens;
+  a.Hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.NB = desc->num_blocks;
+  cudaError_t e = pkv::launch_append(a, kind_of(desc->cache_dtype), kv_dtype == PKV_BF16,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                  int32_t max_blocks_per_seq, int32_t max_context_len_hint) {
+  if (check_desc(desc) != PKV_OK || batch < 0 || max_blocks_per_seq <= 0) return 0;
+  if (batch == 0) return 0;
+  const int sms = sm_count_current_device();
+  if (sms <= 0) return 0;
+  return ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms).total;
+}
+
+pkv_status pkv_paged_decode_attention(const pkv_cache_desc* desc, const void* q,
+                                      const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int32_t batch, int32_t max_blocks_per_seq,
+                                      int32_t max_context_len_hint, float scale, void* out,
+                                      pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || max_blocks_per_seq <= 0 || max_context_len_hint < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * max_blocks_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * kPageSize >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (desc->cache_dtype != PKV_FP8_E4M3 && q_dtype != desc->cache_dtype)
+    return PKV_ERR_INVALID_ARG;
+  if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+    return PKV_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_ERR_INVALID_ARG;
+  const int sms = sm_count_current_device();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms);
+  if (workspace == nullptr || workspace_bytes < w.total || !aligned(workspace, 256))
+    return PKV_ERR_WORKSPACE;
+  const pkv::CacheKind cache = kind_of(desc->cache_dtype);
+  if (pkv::decode_smem_bytes(desc->head_dim, cache, batch) > 227 * 1024)
+    return PKV_ERR_UNSUPPORTED;
+
+  pkv::DecodeLaunch l;
+  st = encode_cache_map(&l.tmap_k, k_cache, desc);
+  if (st != PKV_OK) return st;
+  st = encode_cache_map(&l.tmap_v, v_cache, desc);
+  if (st != PKV_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  l.p.q = q;
+  l.p.block_tables = block_tables;
+  l.p.context_lens = context_lens;
+  l.p.out = out;
+  l.p.part_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  l.p.part_o = reinterpret_cast<float*>(ws + w.o_off);
+  l.p.seg_info = reinterpret_cast<int32_t*>(ws + w.seg_off);
+  l.p.k_scale = desc->k_scale;
+  l.p.v_scale = desc->v_scale;
+  l.p.err_word = desc->err_word;
+  l.p.B = batch;
+  l.p.Hq = desc->num_q_heads;
+  l.p.Hkv = desc->num_kv_heads;
+  l.p.d = desc->head_dim;
+  l.p.NB = desc->num_blocks;
+  l.p.MBS = max_blocks_per_seq;
+  l.p.num_warps_total = w.ctas * pkv::kDecodeWarps;
+  l.p.scale_log2 = scale * 1.4426950408889634f;
+  l.group = desc->num_q_heads / desc->num_kv_heads;
+  l.cache = cache;
+  l.q_bf16 = (q_dtype == PKV_BF16);
+  l.out_dtype = out_dtype;
+  l.ctas = w.ctas;
+  l.stream = reinterpret_cast<cudaStream_t>(stream);
+
+  cudaError_t e;
+  switch (cache) {
+    case pkv::kCacheF16: e = pkv::launch_decode_f16(l); break;
+    case pkv::kCacheBF16: e = pkv::launch_decode_bf16(l); break;
+    default: e = pkv::launch_decode_e4m3(l); break;
+  }
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  e = pkv::launch_combine(l);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+uint64_t pkv_kv_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim,
+                                int32_t elem_bytes) {
+  if (layers < 0 || kv_heads < 0 || head_dim < 0 || elem_bytes < 0) return 0;
+  return 2ull * (uint64_t)layers * (uint64_t)kv_heads * (uint64_t)head_dim *
+         (uint64_t)elem_bytes;
+}
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG: invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: shape or dtype not built";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: CUDA call failed";
+    case PKV_ERR_BOUNDS: return "PKV_ERR_BOUNDS: slot, block id or context length out of range";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT: a bounded device wait gave up";
+  }
+  return "unknown pkv_status";
+}
+
+int32_t pkv_version(void) { return 100; }
+
+}  // extern "C"

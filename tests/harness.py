@@ -1,0 +1,147 @@
+"""Test harness: run a workload through the CUDA path and through the oracle.
+
+The oracle side sees only the logical (unpaged) drawn values and decodes FP8
+bytes with its own codec; the CUDA side sees only the paged pool, the block
+tables and the slot mapping.  Nothing the CUDA path writes is ever fed to the
+oracle.
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_250_gb300 as pkv
+from paged_kv_cache_250_gb300 import workloads as wl
+
+TOL_16BIT = 2e-3   # max abs error vs the oracle, bf16/fp16 cache, fp32 accumulation
+TOL_FP8 = 3e-2     # max abs error vs the oracle on the dequantised cache
+
+_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+_CODE = {"f16": pkv.PKV_F16, "bf16": pkv.PKV_BF16, "e4m3": pkv.PKV_FP8_E4M3}
+
+
+def tolerance(cfg) -> float:
+    return TOL_FP8 if cfg.cache == "e4m3" else TOL_16BIT
+
+
+def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """Half a unit in the last place of `dtype` at |x| (the output rounding)."""
+    mant = {torch.float16: 10, torch.bfloat16: 7, torch.float32: 23}[dtype]
+    emin = {torch.float16: -14, torch.bfloat16: -126, torch.float32: -126}[dtype]
+    ax = np.maximum(np.abs(x), 1e-300)
+    e = np.maximum(np.floor(np.log2(ax)), emin)
+    return 0.5 * np.exp2(e - mant)
+
+
+# ------------------------------------------------------------------ oracle side
+def logical_kv_fp64(w: wl.DecodeWorkload, b: int, h: int) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 K, V rows [ctx][d] of sequence b, KV head h, as the cache holds them
+    after the append: drawn values for 16-bit caches; for E4M3 the stored
+    codes (prefix) or the oracle's own encoding of the new token, decoded and
+    scaled by the oracle's codec."""
+    n = int(w.ctx[b])
+    if w.cfg.cache != "e4m3":
+        K = w.K_log[b, :n, h].double().cpu().numpy()
+        V = w.V_log[b, :n, h].double().cpu().numpy()
+        return K, V
+    ks = float(w.k_scale[h])
+    vs = float(w.v_scale[h])
+    Kc = w.K_stored[b, :n, h].cpu().numpy().copy()
+    Vc = w.V_stored[b, :n, h].cpu().numpy().copy()
+    if n > 0:
+        Kc[n - 1] = oracle.e4m3_quantize(w.k_new[b, h].float().cpu().numpy(), ks)
+        Vc[n - 1] = oracle.e4m3_quantize(w.v_new[b, h].float().cpu().numpy(), vs)
+    return oracle.e4m3_dequantize(Kc, ks), oracle.e4m3_dequantize(Vc, vs)
+
+
+def oracle_rows(w: wl.DecodeWorkload, pairs: Iterable[Tuple[int, int]]) -> dict:
+    """Expected output rows for the given (b, hq) pairs."""
+    g = w.cfg.group
+    res = {}
+    cache = {}
+    for b, hq in pairs:
+        h = hq // g
+        if (b, h) not in cache:
+            cache[(b, h)] = logical_kv_fp64(w, b, h)
+        K, V = cache[(b, h)]
+        q = w.q[b, hq].double().cpu().numpy()
+        res[(b, hq)] = oracle.attend_row(q, K, V, w.cfg.softmax_scale)
+    return res
+
+
+def oracle_all(w: wl.DecodeWorkload) -> np.ndarray:
+    B, Hq, d = w.cfg.batch, w.cfg.q_heads, w.cfg.head_dim
+    out = np.zeros((B, Hq, d))
+    rows = oracle_rows(w, [(b, hq) for b in range(B) for hq in range(Hq)])
+    for (b, hq), r in rows.items():
+        out[b, hq] = r
+    return out
+
+
+# ------------------------------------------------------------------ CUDA side
+class GpuRun:
+    """Device copies of a workload and one append + decode through the C ABI."""
+
+    def __init__(self, w: wl.DecodeWorkload, device="cuda", hint: int = 0,
+                 with_err_word: bool = True):
+        self.w = w
+        cfg = w.cfg
+        self.dev = torch.device(device)
+        self.k_cache = w.k_cache.to(self.dev).contiguous()
+        self.v_cache = w.v_cache.to(self.dev).contiguous()
+        self.q = w.q.to(self.dev).contiguous()
+        self.k_new = w.k_new.to(self.dev).contiguous()
+        self.v_new = w.v_new.to(self.dev).contiguous()
+        self.slot = w.slot_mapping.to(self.dev).contiguous()
+        self.tables = w.block_tables.to(self.dev).contiguous()
+        self.ctx = w.ctx.to(self.dev).contiguous()
+        self.k_scale = None if w.k_scale is None else w.k_scale.to(self.dev).float().contiguous()
+        self.v_scale = None if w.v_scale is None else w.v_scale.to(self.dev).float().contiguous()
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.dev) if with_err_word else None
+        self.desc = pkv.make_desc(w.num_blocks, wl.PAGE, cfg.kv_heads, cfg.q_heads,
+                                  cfg.head_dim, _CODE[cfg.cache], self.k_scale, self.v_scale,
+                                  self.err)
+        self.hint = hint
+        nbytes = pkv.pkv_decode_workspace_bytes(self.desc, cfg.batch, w.max_blocks_per_seq, hint)
+        assert nbytes > 0
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+
+    def append(self):
+        pkv.pkv_kv_append(self.desc, self.k_cache, self.v_cache, self.slot, self.k_new,
+                          self.v_new)
+
+    def decode(self, out_dtype: str = "f32") -> torch.Tensor:
+        cfg = self.w.cfg
+        out = torch.empty(cfg.batch, cfg.q_heads, cfg.head_dim, dtype=_DT[out_dtype],
+                          device=self.dev)
+        pkv.pkv_paged_decode_attention(self.desc, self.q, self.k_cache, self.v_cache,
+                                       self.tables, self.ctx, cfg.softmax_scale, out,
+                                       self.workspace, self.hint)
+        return out
+
+    def step(self, out_dtype: str = "f32") -> torch.Tensor:
+        self.append()
+        return self.decode(out_dtype)
+
+    def err_code(self) -> int:
+        return 0 if self.err is None else int(self.err.item())
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, cfg, out_dtype: str, what: str = ""):
+    """The parity bar: fp32 outputs within the tolerance; 16-bit outputs within
+    the tolerance plus half an output ulp (the output rounding itself)."""
+    tol = tolerance(cfg)
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if out_dtype == "f32":
+        bound = np.full_like(ref, tol)
+    else:
+        bound = tol + half_ulp(ref, _DT[out_dtype])
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of bound; max abs err "
+                           f"{err.max():.3e} (tol {tol})")
+    return float(err.max())

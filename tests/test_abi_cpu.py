@@ -1,0 +1,96 @@
+"""C-ABI library checks that need no GPU: it builds for sm_103a, loads,
+exports every symbol include/pkv.h declares, and its host-only helpers and
+argument validation behave (no compute calls)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_250_gb300 as pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text))
+    return names
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    lib = pkv.load_library()
+    declared = _declared_symbols()
+    assert declared, "no declarations found"
+    assert declared == set(pkv.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    # nothing else is exported with the pkv_ prefix
+    with open(pkv.library_path(), "rb"):
+        pass
+
+
+def test_struct_layout_matches_header():
+    # uint32 + 5 int32 + enum (4 bytes) = 28, padded to 32, then 3 pointers
+    assert ctypes.sizeof(pkv.CacheDesc) == 56
+    assert pkv.CacheDesc.k_scale.offset == 32
+
+
+def test_host_helpers():
+    with open(os.path.join(ROOT, "tests", "golden", "kv_cache_sizes.json")) as f:
+        g = json.load(f)
+    for c in g["bytes_per_token"]:
+        assert pkv.pkv_kv_bytes_per_token(c["layers"], c["kv_heads"], c["head_dim"],
+                                          c["elem_bytes"]) == c["bytes"]
+    assert pkv.pkv_version() >= 100
+    assert "WORKSPACE" in pkv.pkv_status_string(pkv.PKV_ERR_WORKSPACE)
+    assert pkv.pkv_status_string(99) == "unknown pkv_status"
+
+
+def test_argument_errors_return_before_any_launch():
+    lib = pkv.load_library()
+    good = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_BF16)
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    # null cache pointer
+    st = lib.pkv_kv_append(ctypes.byref(good), None, fake, fake, fake, fake, 1, pkv.PKV_BF16, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    # kv dtype must equal a 16-bit cache's dtype
+    st = lib.pkv_kv_append(ctypes.byref(good), fake, fake, fake, fake, fake, 1, pkv.PKV_F16, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    # wrong struct size
+    bad = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_BF16)
+    bad.struct_size = 8
+    st = lib.pkv_kv_append(ctypes.byref(bad), fake, fake, fake, fake, fake, 1, pkv.PKV_BF16, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    # unsupported page size / head dim / group; fp8 without scales
+    for desc in (pkv.make_desc(64, 32, 2, 8, 128, pkv.PKV_BF16),
+                 pkv.make_desc(64, 16, 2, 8, 80, pkv.PKV_BF16),
+                 pkv.make_desc(64, 16, 1, 16, 128, pkv.PKV_BF16),
+                 pkv.make_desc(64, 16, 2, 8, 64, pkv.PKV_FP8_E4M3)):
+        st = lib.pkv_kv_append(ctypes.byref(desc), fake, fake, fake, fake, fake, 1,
+                               pkv.PKV_BF16, None)
+        assert st == pkv.PKV_ERR_UNSUPPORTED
+    nos = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_FP8_E4M3)
+    st = lib.pkv_kv_append(ctypes.byref(nos), fake, fake, fake, fake, fake, 1, pkv.PKV_BF16, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    # zero tokens / zero batch are no-ops
+    assert lib.pkv_kv_append(ctypes.byref(good), None, None, None, None, None, 0,
+                             pkv.PKV_BF16, None) == pkv.PKV_OK
+    assert lib.pkv_paged_decode_attention(ctypes.byref(good), None, None, None, None, None,
+                                          0, 4, 0, 1.0, None, pkv.PKV_BF16, pkv.PKV_BF16,
+                                          None, 0, None) == pkv.PKV_OK
+    # decode: missing pointers, bad dtypes, NaN scale
+    st = lib.pkv_paged_decode_attention(ctypes.byref(good), fake, fake, fake, fake, None, 2, 4, 0,
+                                        1.0, fake, pkv.PKV_BF16, pkv.PKV_BF16, fake, 1 << 20, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    st = lib.pkv_paged_decode_attention(ctypes.byref(good), fake, fake, fake, fake, fake, 2, 4, 0,
+                                        1.0, fake, pkv.PKV_F32, pkv.PKV_BF16, fake, 1 << 20, None)
+    assert st == pkv.PKV_ERR_UNSUPPORTED
+    st = lib.pkv_paged_decode_attention(ctypes.byref(good), fake, fake, fake, fake, fake, 2, 4, 0,
+                                        float("nan"), fake, pkv.PKV_BF16, pkv.PKV_BF16, fake,
+                                        1 << 20, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG

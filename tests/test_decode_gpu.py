@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances: max abs error 2e-3 for bf16/fp16 caches (fp32 output), 3e-2 for
+the E4M3 cache (against the oracle on the dequantised stored bytes); 16-bit
+outputs may add half an output ulp for their own rounding.  Append results
+are compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_250_gb300 as pkv
+from paged_kv_cache_250_gb300 import workloads as wl
+
+from harness import GpuRun, assert_close, oracle_all, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 2, 15, 16, 17, 31, 33, 250, 600, 1000]
+
+
+# ----------------------------------------------------------------- tiny case
+@pytest.mark.parametrize("ctx", [256, 257, 1])
+@pytest.mark.parametrize("out_dtype", ["f32", "f16"])
+def test_tiny_decode_step(ctx, out_dtype):
+    cfg = wl.CONFIGS["tiny_b1_h4x1_d64_f16_ctx256"]
+    w = wl.generate(cfg, ctx_override=torch.tensor([ctx]))
+    run = GpuRun(w)
+    out = run.step(out_dtype).double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    ref = oracle_all(w)
+    err = np.abs(out - ref).max()
+    assert err <= 2e-3, err  # fp16 output meets the raw bound at these magnitudes
+    if ctx == 1:  # a single token: the output is that token's value row
+        v0 = w.v_new[0, 0].float().cpu().numpy()
+        for h in range(4):
+            np.testing.assert_array_equal(out[0, h], v0.astype(np.float64))
+
+
+# ----------------------------------------------------------------- sweep
+@pytest.mark.parametrize("cache", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_ragged_sweep_16bit(cache, d, g):
+    cfg = wl.small_config(f"sweep_{cache}_{d}_{g}", len(RAGGED), 2 * g, 2, d, cache, 1,
+                          seed=11 + g + d)
+    w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
+    run = GpuRun(w)
+    out32 = run.step("f32").double().cpu().numpy()
+    out16 = run.decode(cache).double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    ref = oracle_all(w)
+    assert_close(out32, ref, cfg, "f32", "fp32 out")
+    assert_close(out16, ref, cfg, cache, "16-bit out")
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("q_dtype", ["bf16", "f16"])
+def test_ragged_sweep_fp8(g, q_dtype):
+    cfg = wl.small_config(f"sweep_fp8_{g}", len(RAGGED), 2 * g, 2, 128, "e4m3", 1,
+                          seed=23 + g, q_dtype=q_dtype)
+    w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    out_bf = run.decode("bf16").double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    ref = oracle_all(w)
+    err = assert_close(out, ref, cfg, "f32", "fp8 fp32 out")
+    assert err < 2e-3  # the expected error is far inside the 3e-2 gate
+    assert_close(out_bf, ref, cfg, "bf16", "fp8 bf16 out")
+
+
+def test_many_splits_long_sequence():
+    # one long sequence spread over every warp of the grid, plus short ones
+    cfg = wl.small_config("long", 3, 8, 2, 128, "bf16", 1, seed=5)
+    w = wl.generate(cfg, ctx_override=torch.tensor([20000, 3, 4097]))
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    ref = oracle_all(w)
+    assert_close(out, ref, cfg, "f32", "long")
+
+
+# ----------------------------------------------------------------- append
+@pytest.mark.parametrize("cache", ["f16", "bf16"])
+def test_append_is_bit_exact(cache):
+    cfg = wl.small_config("append", 6, 8, 2, 128, cache, 1, seed=3)
+    w = wl.generate(cfg, ctx_override=torch.tensor([1, 16, 17, 100, 5, 64]))
+    run = GpuRun(w)
+    run.append()
+    torch.cuda.synchronize()
+    view = torch.int16
+    before_k = w.k_cache.view(view).numpy()
+    before_v = w.v_cache.view(view).numpy()
+    exp_k = oracle.append_bytes(before_k, w.k_new.view(view).numpy(), w.slot_mapping.numpy())
+    exp_v = oracle.append_bytes(before_v, w.v_new.view(view).numpy(), w.slot_mapping.numpy())
+    assert np.array_equal(run.k_cache.view(view).cpu().numpy(), exp_k)
+    assert np.array_equal(run.v_cache.view(view).cpu().numpy(), exp_v)
+    assert run.err_code() == 0
+
+
+@pytest.mark.parametrize("scale_kind", ["one", "half", "amax"])
+def test_fp8_append_every_bf16_value(scale_kind):
+    # all 65536 bf16 bit patterns (non-finite ones replaced by 0) as one head
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16)
+    x = bits.view(torch.bfloat16).clone()
+    x[~torch.isfinite(x.float())] = 0
+    T, d = 512, 128
+    k = x.reshape(T, 1, d)
+    v = x.flip(0).reshape(T, 1, d).contiguous()
+    scale = {"one": 1.0, "half": 0.5, "amax": float(x.float().abs().max()) / 448.0}[scale_kind]
+    ks = torch.tensor([scale], dtype=torch.float32)
+    NB = T // 16 + 1
+    dev = "cuda"
+    kc = torch.zeros(NB, 1, 16, d, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    slot = torch.arange(T, dtype=torch.int64) + 16  # skip block 0
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ksd = ks.to(dev)
+    desc = pkv.make_desc(NB, 16, 1, 1, d, pkv.PKV_FP8_E4M3, ksd, ksd, err)
+    pkv.pkv_kv_append(desc, kc, vc, slot.to(dev), k.to(dev), v.to(dev))
+    torch.cuda.synchronize()
+    exp_k = oracle.append_e4m3(np.zeros((NB, 1, 16, d), np.uint8), k.float().numpy(),
+                               slot.numpy(), ks.numpy())
+    exp_v = oracle.append_e4m3(np.zeros((NB, 1, 16, d), np.uint8), v.float().numpy(),
+                               slot.numpy(), ks.numpy())
+    got_k, got_v = kc.cpu().numpy(), vc.cpu().numpy()
+    # +0 and -0 both decode to zero; compare the rest bit for bit
+    zk = (exp_k & 0x7F) == 0
+    assert np.array_equal(got_k[~zk], exp_k[~zk]) and np.all((got_k[zk] & 0x7F) == 0)
+    zv = (exp_v & 0x7F) == 0
+    assert np.array_equal(got_v[~zv], exp_v[~zv]) and np.all((got_v[zv] & 0x7F) == 0)
+    assert int(err.item()) == 0
+
+
+def test_append_skips_negative_slots_and_reports_out_of_pool():
+    cfg = wl.small_config("oob", 3, 4, 1, 64, "f16", 1, seed=2)
+    w = wl.generate(cfg, ctx_override=torch.tensor([5, 7, 9]))
+    slot = w.slot_mapping.clone()
+    slot[0] = -1
+    slot[2] = w.num_blocks * 16 + 3  # past the pool
+    w.slot_mapping = slot
+    run = GpuRun(w)
+    run.append()
+    torch.cuda.synchronize()
+    view = torch.int16
+    exp = oracle.append_bytes(w.k_cache.view(view).numpy(), w.k_new.view(view).numpy(),
+                              slot.numpy())
+    assert np.array_equal(run.k_cache.view(view).cpu().numpy(), exp)
+    assert run.err_code() == pkv.PKV_ERR_BOUNDS
+
+
+# ----------------------------------------------------------------- invariants
+def test_paging_is_invisible_to_the_result():
+    ctx = torch.tensor([40, 300, 17, 1, 129])
+    outs = []
+    for table in ("identity", "permuted"):
+        cfg = wl.DecodeConfig("inv", 5, 8, 2, 128, "bf16", 1, table=table, seed=9,
+                              spare_blocks=7)
+        w = wl.generate(cfg, ctx_override=ctx)
+        run = GpuRun(w)
+        outs.append(run.step("f32").cpu())
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_repeatable_and_zero_context_rows():
+    cfg = wl.small_config("zero", 5, 8, 2, 128, "bf16", 1, seed=4)
+    w = wl.generate(cfg, ctx_override=torch.tensor([0, 33, 0, 1, 500]))
+    run = GpuRun(w)
+    run.append()
+    a = run.decode("f32").cpu()
+    b = run.decode("f32").cpu()
+    assert torch.equal(a, b)
+    assert torch.all(a[0] == 0) and torch.all(a[2] == 0)
+    ref = oracle_all(w)
+    assert_close(a.double().numpy(), ref, cfg, "f32", "zero-ctx batch")
+    allzero = wl.generate(cfg, ctx_override=torch.tensor([0, 0, 0, 0, 0]))
+    run0 = GpuRun(allzero)
+    assert torch.all(run0.decode("bf16") == 0)
+
+
+def test_prefix_sharing_tables():
+    # sequence 1 shares sequence 0's first 3 blocks (48 tokens), then diverges
+    cfg = wl.small_config("share", 2, 8, 2, 64, "f16", 1, seed=8, spare_blocks=0)
+    w = wl.generate(cfg, ctx_override=torch.tensor([60, 70]))
+    tables = w.block_tables.clone()
+    tables[1, :3] = tables[0, :3]
+    w.block_tables = tables
+    # the logical view of sequence 1 now starts with sequence 0's tokens
+    w.K_log[1, :48] = w.K_log[0, :48]
+    w.V_log[1, :48] = w.V_log[0, :48]
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    ref = oracle_all(w)
+    assert_close(out, ref, cfg, "f32", "shared prefix")
+
+
+def test_bad_block_table_entry_is_reported_not_read():
+    cfg = wl.small_config("badtab", 3, 8, 2, 128, "bf16", 1, seed=6)
+    w = wl.generate(cfg, ctx_override=torch.tensor([40, 40, 40]))
+    tables = w.block_tables.clone()
+    tables[1, 1] = w.num_blocks + 100
+    w.block_tables = tables
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == pkv.PKV_ERR_BOUNDS
+    ref = oracle_all(w)
+    for b in (0, 2):
+        assert np.abs(out[b] - ref[b]).max() <= 2e-3
+    assert np.all(np.isfinite(out[1]))
+
+
+def test_host_side_argument_errors():
+    cfg = wl.small_config("args", 2, 8, 2, 128, "bf16", 1, seed=1)
+    w = wl.generate(cfg, ctx_override=torch.tensor([5, 6]))
+    run = GpuRun(w)
+    out = torch.empty(2, 8, 128, dtype=torch.float32, device="cuda")
+    small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_paged_decode_attention(run.desc, run.q, run.k_cache, run.v_cache, run.tables,
+                                       run.ctx, 0.1, out, small_ws)
+    assert e.value.status == pkv.PKV_ERR_WORKSPACE
+    with pytest.raises(pkv.PkvError) as e:  # q dtype must match a 16-bit cache
+        pkv.pkv_paged_decode_attention(run.desc, run.q.half(), run.k_cache, run.v_cache,
+                                       run.tables, run.ctx, 0.1, out, run.workspace)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    bad = pkv.make_desc(w.num_blocks, 16, 3, 8, 128, pkv.PKV_BF16)  # 8 % 3 != 0
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_paged_decode_attention(bad, run.q, run.k_cache, run.v_cache, run.tables,
+                                       run.ctx, 0.1, out, run.workspace)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    unsup = pkv.make_desc(w.num_blocks, 16, 2, 8, 96, pkv.PKV_BF16)
+    assert pkv.pkv_decode_workspace_bytes(unsup, 2, 1) == 0
+
+
+# ----------------------------------------------------------------- full sizes
+FULL = [n for n in wl.CONFIGS if not n.startswith("tiny")]
+BENCH_HINT = {"llama3_8b_b32_ctx1-4096_bf16": 4096}
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_configs_sampled(name):
+    cfg = wl.CONFIGS[name]
+    w = wl.generate(cfg, device="cuda")
+    run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
+    out = run.step("bf16" if cfg.cache != "f16" else "f16").double().cpu().numpy()
+    out32 = run.decode("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    assert np.all(np.isfinite(out32))
+    rng = np.random.default_rng(cfg.seed)
+    ctx = w.ctx.numpy()
+    bs = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), 0, cfg.batch - 1,
+                 *rng.integers(0, cfg.batch, 4).tolist()})
+    pairs = [(b, int(hq)) for b in bs for hq in rng.choice(cfg.q_heads, 3, replace=False)]
+    ref = oracle_rows(w, pairs)
+    r = np.stack([ref[p] for p in pairs])
+    assert_close(np.stack([out32[b, hq] for b, hq in pairs]), r, cfg, "f32", name)
+    assert_close(np.stack([out[b, hq] for b, hq in pairs]), r, cfg,
+                 "bf16" if cfg.cache != "f16" else "f16", name)
