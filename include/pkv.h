@@ -105,10 +105,14 @@ PKV_API pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache,
                          const void* k, const void* v, int32_t num_tokens,
                          pkv_dtype kv_dtype, pkv_stream_t stream);
 
-/* Bytes of device workspace pkv_paged_decode_attention needs for these
- * sizes on the current device (it depends on the SM count).  Returns 0 on
- * invalid arguments.  The workspace holds the split partials and a per-
- * (sequence, KV head) split count; its contents need no initialisation. */
+/* Bytes of device workspace pkv_paged_decode_attention / pkv_decode_step
+ * need for these sizes on the current device (it depends on the SM count).
+ * Returns 0 on invalid arguments or without a device.  The workspace holds
+ * one arrival counter per (sequence, KV head) and the split partials.  It
+ * must be zero-filled once before its first use (e.g. cudaMemsetAsync);
+ * every call that completes leaves the counters at zero again, so it can be
+ * reused without clearing.  After a call that reported PKV_ERR_TIMEOUT,
+ * zero it again.  Calls that share a workspace must not overlap. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t max_blocks_per_seq,
                                   int32_t max_context_len_hint);
@@ -135,7 +139,12 @@ PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t ba
  *   out           [batch][num_q_heads][head_dim] of out_dtype (F16 | BF16 |
  *                 F32), rounded to nearest even.  Must not alias inputs.
  *   workspace     device buffer of at least pkv_decode_workspace_bytes(),
- *                 256-byte aligned; not shared with concurrent calls.  */
+ *                 256-byte aligned, zero-filled before its first use (see
+ *                 pkv_decode_workspace_bytes); not shared with concurrent
+ *                 calls.
+ * The kernel is launched as a programmatic dependent of the preceding
+ * kernel on the stream but waits for it to complete before reading any
+ * input, so ordinary stream order holds. */
 PKV_API pkv_status pkv_paged_decode_attention(
     const pkv_cache_desc* desc, const void* q, const void* k_cache,
     const void* v_cache, const int32_t* block_tables,
@@ -143,6 +152,22 @@ PKV_API pkv_status pkv_paged_decode_attention(
     int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
     pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
     pkv_stream_t stream);
+
+/* One whole decode step: pkv_kv_append of one new token per sequence
+ * (slot_mapping, k, v have `batch` rows) followed by
+ * pkv_paged_decode_attention, validated together before anything is
+ * launched.  The attention kernel is launched as a programmatic dependent
+ * of the append kernel: it reads context_lens and block_tables and plans
+ * its work while the append runs, and waits for the append to complete
+ * before reading any cache page.  context_lens must already count the
+ * appended token.  Arguments as for the two calls above. */
+PKV_API pkv_status pkv_decode_step(
+    const pkv_cache_desc* desc, const void* q, void* k_cache, void* v_cache,
+    const int64_t* slot_mapping, const void* k, const void* v, pkv_dtype kv_dtype,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t batch,
+    int32_t max_blocks_per_seq, int32_t max_context_len_hint, float scale,
+    void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
 
 /* Cache bytes per token across all layers: 2 * layers * kv_heads * head_dim
  * * elem_bytes ([AP] "Opening the hood: how big is the notebook?"; [DF]

@@ -7,6 +7,8 @@ memory and streams.  The functions carry the C names:
     pkv_kv_append                 write new K/V rows into their cache slots
     pkv_decode_workspace_bytes    workspace size for a decode call
     pkv_paged_decode_attention    one (1,N) attention row per query head
+    pkv_decode_step               both, validated together, the attention
+                                  kernel overlapping the append's tail
     pkv_kv_bytes_per_token        cache bytes per token (host helper)
     pkv_status_string, pkv_version
 
@@ -28,7 +30,7 @@ from . import build as _build
 __all__ = [
     "PkvError", "CacheDesc", "make_desc", "load_library", "library_path",
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
-    "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
+    "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
     "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "EXPORTED_SYMBOLS",
@@ -40,7 +42,7 @@ PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
 
 EXPORTED_SYMBOLS = (
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
-    "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
+    "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
 )
 
 _DTYPE_CODE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16,
@@ -96,6 +98,9 @@ def load_library():
         lib.pkv_paged_decode_attention.restype = I32
         lib.pkv_paged_decode_attention.argtypes = [D, P, P, P, P, P, I32, I32, I32,
                                                    ctypes.c_float, P, I32, I32, P, SZ, P]
+        lib.pkv_decode_step.restype = I32
+        lib.pkv_decode_step.argtypes = [D, P, P, P, P, P, P, I32, P, P, I32, I32, I32,
+                                        ctypes.c_float, P, I32, I32, P, SZ, P]
         lib.pkv_kv_bytes_per_token.restype = U64
         lib.pkv_kv_bytes_per_token.argtypes = [I32, I32, I32, I32]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -196,6 +201,32 @@ def pkv_paged_decode_attention(desc: CacheDesc, q: torch.Tensor, k_cache: torch.
     _check(st, "pkv_paged_decode_attention")
 
 
+def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
+                    v_cache: torch.Tensor, slot_mapping: torch.Tensor, k: torch.Tensor,
+                    v: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                    scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                    max_context_len_hint: int = 0, stream=None) -> None:
+    """Append one token per sequence (k, v: [B][Hkv][d]) then attend."""
+    lib = load_library()
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    B, mbs = int(block_tables.shape[0]), int(block_tables.shape[1])
+    if k.shape[0] != B or v.shape != k.shape or slot_mapping.shape[0] != B:
+        raise ValueError("k, v and slot_mapping need one row per sequence")
+    st = lib.pkv_decode_step(
+        ctypes.byref(desc), _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), _dev_ptr(slot_mapping, "slot_mapping"),
+        _dev_ptr(k, "k"), _dev_ptr(v, "v"), _DTYPE_CODE.get(k.dtype, -1),
+        _dev_ptr(block_tables, "block_tables"), _dev_ptr(context_lens, "context_lens"),
+        B, mbs, int(max_context_len_hint), float(scale), _dev_ptr(out, "out"),
+        _DTYPE_CODE.get(q.dtype, -1), _DTYPE_CODE.get(out.dtype, -1),
+        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
+        _stream_handle(stream, q.device))
+    _check(st, "pkv_decode_step")
+
+
 def pkv_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
     return int(load_library().pkv_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes))
 
@@ -210,7 +241,7 @@ def pkv_version() -> int:
 
 @dataclass
 class DecodeBuffers:
-    """Workspace sized for a launch shape (convenience for callers)."""
+    """Zero-filled workspace sized for a launch shape (convenience for callers)."""
     workspace: torch.Tensor
 
     @staticmethod
@@ -219,4 +250,4 @@ class DecodeBuffers:
         n = pkv_decode_workspace_bytes(desc, batch, max_blocks_per_seq, max_context_len_hint)
         if n == 0:
             raise PkvError(PKV_ERR_INVALID_ARG, "pkv_decode_workspace_bytes")
-        return DecodeBuffers(torch.empty(n, dtype=torch.uint8, device=device))
+        return DecodeBuffers(torch.zeros(n, dtype=torch.uint8, device=device))

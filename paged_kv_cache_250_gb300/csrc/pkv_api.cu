@@ -80,30 +80,35 @@ pkv::CacheKind kind_of(pkv_dtype t) {
 }
 
 struct WsLayout {
-  size_t ml_off, o_off, seg_off, total;
+  size_t ticket_off, ml_off, o_off, total;
   int ctas;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Workspace: per-segment arrival tickets (must start at zero; the kernel
+// returns them to zero), then the split partials, one slot per possible
+// chunk id (cta + segment).
 WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t hint,
                    int num_sms) {
   const int64_t g = d->num_q_heads / d->num_kv_heads;
   const int64_t cap = (int64_t)mbs * kPageSize;
   const int64_t len = (hint > 0 && hint < cap) ? hint : cap;
-  const int64_t pages_bound = (int64_t)batch * d->num_kv_heads * ((len + kPageSize - 1) / kPageSize);
+  const int64_t pages_bound =
+      (int64_t)batch * d->num_kv_heads * ((len + kPageSize - 1) / kPageSize);
   // at least two pages per warp; at most kDecodeCtasPerSm CTAs per SM
   int64_t ctas = (pages_bound + 2 * pkv::kDecodeWarps - 1) / (2 * pkv::kDecodeWarps);
   const int64_t max_ctas = (int64_t)num_sms * pkv::kDecodeCtasPerSm;
   if (ctas > max_ctas) ctas = max_ctas;
   if (ctas < 1) ctas = 1;
-  const int64_t chunks = ctas * pkv::kDecodeWarps + (int64_t)batch * d->num_kv_heads;
+  const int64_t segs = (int64_t)batch * d->num_kv_heads;
+  const int64_t chunks = ctas + segs;
   WsLayout w;
   w.ctas = (int)ctas;
-  w.ml_off = 0;
+  w.ticket_off = 0;
+  w.ml_off = align256((size_t)segs * sizeof(int32_t));
   w.o_off = align256(w.ml_off + (size_t)chunks * g * 2 * sizeof(float));
-  w.seg_off = align256(w.o_off + (size_t)chunks * g * d->head_dim * sizeof(float));
-  w.total = align256(w.seg_off + (size_t)batch * d->num_kv_heads * 2 * sizeof(int32_t));
+  w.total = align256(w.o_off + (size_t)chunks * g * d->head_dim * sizeof(float));
   return w;
 }
 
@@ -124,6 +129,107 @@ pkv_status encode_cache_map(CUtensorMap* map, const void* cache, const pkv_cache
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status append_checks(const pkv_cache_desc* desc, const void* k_cache, const void* v_cache,
+                         const int64_t* slot_mapping, const void* k, const void* v,
+                         int32_t num_tokens, pkv_dtype kv_dtype) {
+  if (!k_cache || !v_cache || !slot_mapping || !k || !v) return PKV_ERR_INVALID_ARG;
+  if (kv_dtype != PKV_F16 && kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (desc->cache_dtype != PKV_FP8_E4M3 && kv_dtype != desc->cache_dtype)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(slot_mapping, 8))
+    return PKV_ERR_INVALID_ARG;
+  (void)num_tokens;
+  return PKV_OK;
+}
+
+pkv_status decode_checks(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
+                         int32_t max_context_len_hint, float scale, const void* out,
+                         pkv_dtype q_dtype, pkv_dtype out_dtype, const void* workspace,
+                         size_t workspace_bytes) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || max_blocks_per_seq <= 0 || max_context_len_hint < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * max_blocks_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * kPageSize >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (desc->cache_dtype != PKV_FP8_E4M3 && q_dtype != desc->cache_dtype)
+    return PKV_ERR_INVALID_ARG;
+  if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+    return PKV_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_ERR_INVALID_ARG;
+  const pkv::CacheKind cache = kind_of(desc->cache_dtype);
+  if (pkv::decode_smem_bytes(desc->head_dim, cache, batch) > 227 * 1024)
+    return PKV_ERR_UNSUPPORTED;
+  const int sms = sm_count_current_device();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms);
+  if (workspace == nullptr || workspace_bytes < w.total || !aligned(workspace, 256))
+    return PKV_ERR_WORKSPACE;
+  return PKV_OK;
+}
+
+pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables,
+                       const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
+                       int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
+                       pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                       pkv_stream_t stream, int early_prologue) {
+  pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                                max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
+                                out_dtype, workspace, workspace_bytes);
+  if (st != PKV_OK || batch == 0) return st;
+  const int sms = sm_count_current_device();
+  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms);
+  pkv::DecodeLaunch l;
+  st = encode_cache_map(&l.tmap_k, k_cache, desc);
+  if (st != PKV_OK) return st;
+  st = encode_cache_map(&l.tmap_v, v_cache, desc);
+  if (st != PKV_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  l.p.q = q;
+  l.p.block_tables = block_tables;
+  l.p.context_lens = context_lens;
+  l.p.out = out;
+  l.p.tickets = reinterpret_cast<int32_t*>(ws + w.ticket_off);
+  l.p.part_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  l.p.part_o = reinterpret_cast<float*>(ws + w.o_off);
+  l.p.k_scale = desc->k_scale;
+  l.p.v_scale = desc->v_scale;
+  l.p.err_word = desc->err_word;
+  l.p.B = batch;
+  l.p.Hq = desc->num_q_heads;
+  l.p.Hkv = desc->num_kv_heads;
+  l.p.d = desc->head_dim;
+  l.p.NB = desc->num_blocks;
+  l.p.MBS = max_blocks_per_seq;
+  l.p.out_dtype = out_dtype;
+  l.p.early_prologue = early_prologue;
+  l.p.scale_log2 = scale * 1.4426950408889634f;
+  l.group = desc->num_q_heads / desc->num_kv_heads;
+  l.cache = kind_of(desc->cache_dtype);
+  l.q_bf16 = (q_dtype == PKV_BF16);
+  l.ctas = w.ctas;
+  l.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (l.cache) {
+    case pkv::kCacheF16: e = pkv::launch_decode_f16(l); break;
+    case pkv::kCacheBF16: e = pkv::launch_decode_bf16(l); break;
+    default: e = pkv::launch_decode_e4m3(l); break;
+  }
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -135,13 +241,8 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
   if (st != PKV_OK) return st;
   if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
-  if (!k_cache || !v_cache || !slot_mapping || !k || !v) return PKV_ERR_INVALID_ARG;
-  if (kv_dtype != PKV_F16 && kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (desc->cache_dtype != PKV_FP8_E4M3 && kv_dtype != desc->cache_dtype)
-    return PKV_ERR_INVALID_ARG;
-  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k, 16) || !aligned(v, 16) ||
-      !aligned(slot_mapping, 8))
-    return PKV_ERR_INVALID_ARG;
+  st = append_checks(desc, k_cache, v_cache, slot_mapping, k, v, num_tokens, kv_dtype);
+  if (st != PKV_OK) return st;
   pkv::AppendParams a;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
@@ -176,74 +277,32 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* desc, const void* q,
                                       int32_t max_context_len_hint, float scale, void* out,
                                       pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
                                       size_t workspace_bytes, pkv_stream_t stream) {
-  pkv_status st = check_desc(desc);
-  if (st != PKV_OK) return st;
-  if (batch < 0 || max_blocks_per_seq <= 0 || max_context_len_hint < 0)
-    return PKV_ERR_INVALID_ARG;
-  if (batch == 0) return PKV_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return PKV_ERR_INVALID_ARG;
-  if ((int64_t)batch * max_blocks_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
-  if ((int64_t)max_blocks_per_seq * kPageSize >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
-  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (desc->cache_dtype != PKV_FP8_E4M3 && q_dtype != desc->cache_dtype)
-    return PKV_ERR_INVALID_ARG;
-  if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
-    return PKV_ERR_UNSUPPORTED;
-  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4))
-    return PKV_ERR_INVALID_ARG;
-  const int sms = sm_count_current_device();
-  if (sms <= 0) return PKV_ERR_CUDA;
-  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms);
-  if (workspace == nullptr || workspace_bytes < w.total || !aligned(workspace, 256))
-    return PKV_ERR_WORKSPACE;
-  const pkv::CacheKind cache = kind_of(desc->cache_dtype);
-  if (pkv::decode_smem_bytes(desc->head_dim, cache, batch) > 227 * 1024)
-    return PKV_ERR_UNSUPPORTED;
+  return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                     max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                     workspace, workspace_bytes, stream, /*early_prologue=*/0);
+}
 
-  pkv::DecodeLaunch l;
-  st = encode_cache_map(&l.tmap_k, k_cache, desc);
+pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, void* k_cache,
+                           void* v_cache, const int64_t* slot_mapping, const void* k,
+                           const void* v, pkv_dtype kv_dtype, const int32_t* block_tables,
+                           const int32_t* context_lens, int32_t batch,
+                           int32_t max_blocks_per_seq, int32_t max_context_len_hint,
+                           float scale, void* out, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                           void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  // Validate everything before the first launch, so an error launches nothing.
+  pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                                max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
+                                out_dtype, workspace, workspace_bytes);
   if (st != PKV_OK) return st;
-  st = encode_cache_map(&l.tmap_v, v_cache, desc);
-  if (st != PKV_OK) return st;
-  char* ws = static_cast<char*>(workspace);
-  l.p.q = q;
-  l.p.block_tables = block_tables;
-  l.p.context_lens = context_lens;
-  l.p.out = out;
-  l.p.part_ml = reinterpret_cast<float*>(ws + w.ml_off);
-  l.p.part_o = reinterpret_cast<float*>(ws + w.o_off);
-  l.p.seg_info = reinterpret_cast<int32_t*>(ws + w.seg_off);
-  l.p.k_scale = desc->k_scale;
-  l.p.v_scale = desc->v_scale;
-  l.p.err_word = desc->err_word;
-  l.p.B = batch;
-  l.p.Hq = desc->num_q_heads;
-  l.p.Hkv = desc->num_kv_heads;
-  l.p.d = desc->head_dim;
-  l.p.NB = desc->num_blocks;
-  l.p.MBS = max_blocks_per_seq;
-  l.p.num_warps_total = w.ctas * pkv::kDecodeWarps;
-  l.p.scale_log2 = scale * 1.4426950408889634f;
-  l.group = desc->num_q_heads / desc->num_kv_heads;
-  l.cache = cache;
-  l.q_bf16 = (q_dtype == PKV_BF16);
-  l.out_dtype = out_dtype;
-  l.ctas = w.ctas;
-  l.stream = reinterpret_cast<cudaStream_t>(stream);
-
-  cudaError_t e;
-  switch (cache) {
-    case pkv::kCacheF16: e = pkv::launch_decode_f16(l); break;
-    case pkv::kCacheBF16: e = pkv::launch_decode_bf16(l); break;
-    default: e = pkv::launch_decode_e4m3(l); break;
+  if (batch > 0) {
+    st = append_checks(desc, k_cache, v_cache, slot_mapping, k, v, batch, kv_dtype);
+    if (st != PKV_OK) return st;
   }
-  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
-  if (e != cudaSuccess) return PKV_ERR_CUDA;
-  e = pkv::launch_combine(l);
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  st = pkv_kv_append(desc, k_cache, v_cache, slot_mapping, k, v, batch, kv_dtype, stream);
+  if (st != PKV_OK) return st;
+  return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                     max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                     workspace, workspace_bytes, stream, /*early_prologue=*/1);
 }
 
 uint64_t pkv_kv_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim,

@@ -1,0 +1,81 @@
+// Append/scatter kernel.
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Append / scatter.  One thread moves 8 elements (16 bytes) of one (token,
+// KV head) row of K and the same of V into slot_mapping[token]: block =
+// slot / P, offset = slot % P ("KV Cache & Flash Attention."
+// (kvcache-7e2.pages.dev), PagedAttention section).  Negative slots are
+// skipped; slots past the pool are reported, never written.  For an E4M3
+// cache each value is divided by its head's scale (IEEE fp32) and encoded
+// round-to-nearest-even with saturation to +-448.
+template <bool IN_BF16>
+__device__ __forceinline__ uint2 quantize8(uint4 in, float scale) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t outw[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 a = unpack2<IN_BF16>(w[2 * i]);
+    const float2 b = unpack2<IN_BF16>(w[2 * i + 1]);
+    const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
+    const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale));
+    outw[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return make_uint2(outw[0], outw[1]);
+}
+
+template <int CACHE, bool IN_BF16>
+__global__ void append_kernel(const AppendParams a) {
+  // let a dependent decode kernel start its prologue while this one runs
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int per_row = a.d >> 3;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = tid / per_row;
+  if (row >= (int64_t)a.T * a.Hkv) return;
+  const int part = (int)(tid - row * per_row);
+  const int t = (int)(row / a.Hkv);
+  const int h = (int)(row - (int64_t)t * a.Hkv);
+  const int64_t slot = a.slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= (int64_t)a.NB * kPageSize) {
+    if (part == 0) report_error(a.err_word, PKV_ERR_BOUNDS);
+    return;
+  }
+  const int64_t blk = slot / kPageSize;
+  const int64_t off = slot - blk * kPageSize;
+  const int64_t dst = ((blk * a.Hkv + h) * kPageSize + off) * per_row + part;
+  const uint4 kin = reinterpret_cast<const uint4*>(a.k)[row * per_row + part];
+  const uint4 vin = reinterpret_cast<const uint4*>(a.v)[row * per_row + part];
+  if constexpr (CACHE != kCacheE4M3) {
+    reinterpret_cast<uint4*>(a.k_cache)[dst] = kin;
+    reinterpret_cast<uint4*>(a.v_cache)[dst] = vin;
+  } else {
+    reinterpret_cast<uint2*>(a.k_cache)[dst] = quantize8<IN_BF16>(kin, a.k_scale[h]);
+    reinterpret_cast<uint2*>(a.v_cache)[dst] = quantize8<IN_BF16>(vin, a.v_scale[h]);
+  }
+}
+
+cudaError_t launch_append(const AppendParams& a, CacheKind cache, bool in_bf16,
+                          cudaStream_t stream) {
+  const int64_t threads_total = (int64_t)a.T * a.Hkv * (a.d / 8);
+  if (threads_total == 0) return cudaSuccess;
+  const int block = 256;
+  const int64_t grid = (threads_total + block - 1) / block;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  if (cache == kCacheE4M3) {
+    if (in_bf16)
+      append_kernel<kCacheE4M3, true><<<(unsigned)grid, block, 0, stream>>>(a);
+    else
+      append_kernel<kCacheE4M3, false><<<(unsigned)grid, block, 0, stream>>>(a);
+  } else {
+    append_kernel<kCacheBF16, false><<<(unsigned)grid, block, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -16,21 +16,40 @@ constexpr int kDecodeCtasPerSm = 2;
 
 enum CacheKind { kCacheF16 = 0, kCacheBF16 = 1, kCacheE4M3 = 2 };
 
-// Arguments of the split kernel (one warp = one contiguous share of all
-// (sequence, KV head, page) units) and of the split-combine kernel.
+// Shared-memory plan of the decode kernel (host and device agree on it).
+constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
+constexpr int decode_stage_bytes(int d, CacheKind c) {
+  return 2 * kPageSize * d * (c == kCacheE4M3 ? 1 : 2);
+}
+// alignment slack + descriptor windows + merge buffers + flag + mbarriers (8 max)
+constexpr int decode_fixed_smem(int d) {
+  return 1024 + kDecodeWarps * 64 * 16 + 2 * decode_lane_state(d) * 32 * 4 + 16 +
+         kDecodeWarps * 8 * 8;
+}
+// Ring depth: as many K+V page slots per warp as fit two CTAs per SM with
+// room for a 256-sequence prefix array; between 2 and 8.
+constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
+constexpr int decode_stages(int d, CacheKind c) {
+  return decode_clamp_stages((112 * 1024 - decode_fixed_smem(d) - 2 * 1024) /
+                             (kDecodeWarps * decode_stage_bytes(d, c)));
+}
+
+// Arguments of the decode kernel (one CTA = one contiguous share of all
+// (sequence, KV head, page) units; split partials merged in-kernel).
 struct DecodeParams {
   const void* q;               // [B][Hq][d]
   const int32_t* block_tables; // [B][MBS]
   const int32_t* context_lens; // [B]
   void* out;                   // [B][Hq][d]
   float* part_o;               // [chunks][G][d]   unnormalised partial outputs
-  float* part_ml;              // [chunks][G][2]   (running max in log2 units, sum)
-  int32_t* seg_info;           // [B*Hkv][2]       (first chunk id, chunk count)
+  float* part_ml;              // [chunks][G][2]   (reference max in log2 units, sum)
+  int32_t* tickets;            // [B*Hkv]          arrivals per segment; zero between calls
   const float* k_scale;        // FP8 only
   const float* v_scale;        // FP8 only
   int32_t* err_word;
   int32_t B, Hq, Hkv, d, NB, MBS;
-  int32_t num_warps_total;     // warps in the split launch
+  pkv_dtype out_dtype;
+  int32_t early_prologue;      // 1: read lengths/tables before waiting on the previous kernel
   float scale_log2;            // softmax scale * log2(e)
 };
 
@@ -41,7 +60,6 @@ struct DecodeLaunch {
   int32_t group;               // Hq / Hkv
   CacheKind cache;
   bool q_bf16;
-  pkv_dtype out_dtype;
   int32_t ctas;
   cudaStream_t stream;
 };
@@ -59,14 +77,17 @@ struct AppendParams {
 };
 
 // Dynamic shared memory the split kernel needs for a batch of B sequences.
-size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B);
+inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
+  return (size_t)decode_fixed_smem(d) +
+         (size_t)kDecodeWarps * decode_stages(d, cache) * decode_stage_bytes(d, cache) +
+         (size_t)(2 * B + 1) * 4;
+}
 
-// Returns a CUDA error (cudaSuccess when both kernels were enqueued) or
+// Returns a CUDA error (cudaSuccess when the kernel was enqueued) or
 // cudaErrorNotSupported when no kernel is built for the combination.
 cudaError_t launch_decode_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_e4m3(const DecodeLaunch& l);
-cudaError_t launch_combine(const DecodeLaunch& l);
 cudaError_t launch_append(const AppendParams& a, CacheKind cache, bool in_bf16,
                           cudaStream_t stream);
 

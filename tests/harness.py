@@ -108,7 +108,7 @@ class GpuRun:
         self.hint = hint
         nbytes = pkv.pkv_decode_workspace_bytes(self.desc, cfg.batch, w.max_blocks_per_seq, hint)
         assert nbytes > 0
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.dev)
 
     def append(self):
         pkv.pkv_kv_append(self.desc, self.k_cache, self.v_cache, self.slot, self.k_new,
@@ -123,9 +123,18 @@ class GpuRun:
                                        self.workspace, self.hint)
         return out
 
-    def step(self, out_dtype: str = "f32") -> torch.Tensor:
-        self.append()
-        return self.decode(out_dtype)
+    def step(self, out_dtype: str = "f32", fused: bool = True) -> torch.Tensor:
+        """One decode step; fused uses pkv_decode_step, else the two calls."""
+        if not fused:
+            self.append()
+            return self.decode(out_dtype)
+        cfg = self.w.cfg
+        out = torch.empty(cfg.batch, cfg.q_heads, cfg.head_dim, dtype=_DT[out_dtype],
+                          device=self.dev)
+        pkv.pkv_decode_step(self.desc, self.q, self.k_cache, self.v_cache, self.slot,
+                            self.k_new, self.v_new, self.tables, self.ctx, cfg.softmax_scale,
+                            out, self.workspace, self.hint)
+        return out
 
     def err_code(self) -> int:
         return 0 if self.err is None else int(self.err.item())

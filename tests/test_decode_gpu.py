@@ -43,12 +43,13 @@ def test_tiny_decode_step(ctx, out_dtype):
 @pytest.mark.parametrize("cache", ["f16", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
-def test_ragged_sweep_16bit(cache, d, g):
+@pytest.mark.parametrize("fused", [True, False])
+def test_ragged_sweep_16bit(cache, d, g, fused):
     cfg = wl.small_config(f"sweep_{cache}_{d}_{g}", len(RAGGED), 2 * g, 2, d, cache, 1,
                           seed=11 + g + d)
     w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
     run = GpuRun(w)
-    out32 = run.step("f32").double().cpu().numpy()
+    out32 = run.step("f32", fused=fused).double().cpu().numpy()
     out16 = run.decode(cache).double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
