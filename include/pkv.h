@@ -169,6 +169,35 @@ PKV_API pkv_status pkv_decode_step(
     void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
     size_t workspace_bytes, pkv_stream_t stream);
 
+/* Size of the fixed device scratch behind pkv_paged_decode_attention_noalloc
+ * (32 MiB, held by every GPU that loads the library until the process ends). */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* pkv_paged_decode_attention without a caller workspace.  The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory when they attend (a custom-op hook with no allocator handle, a plugin
+ * inside an engine that owns all device memory, a path that must not call
+ * cudaMalloc because it may synchronise the device).  It runs the same kernel
+ * on a fixed scratch array in the library's own device image and allocates
+ * nothing.
+ *   - Shapes whose workspace (pkv_decode_workspace_bytes) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE; other argument
+ *     errors are those of pkv_paged_decode_attention.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress); make that first call before any stream
+ *     capture on that device.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; each call first clears, on `stream`, the part that must start
+ *     at zero.  Calls whose executions overlap on the GPU (other streams,
+ *     other threads) race on the scratch and give wrong results: order them.
+ * Arguments otherwise as for pkv_paged_decode_attention. */
+PKV_API pkv_status pkv_paged_decode_attention_noalloc(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
+    int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
+    pkv_dtype out_dtype, pkv_stream_t stream);
+
 /* Cache bytes per token across all layers: 2 * layers * kv_heads * head_dim
  * * elem_bytes ([AP] "Opening the hood: how big is the notebook?"; [DF]
  * cache-size paragraph).  Host-only. */

@@ -31,6 +31,7 @@ __all__ = [
     "PkvError", "CacheDesc", "make_desc", "load_library", "library_path",
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
+    "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
     "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "EXPORTED_SYMBOLS",
@@ -43,7 +44,9 @@ PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
 EXPORTED_SYMBOLS = (
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
+    "pkv_paged_decode_attention_noalloc",
 )
+PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _DTYPE_CODE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16,
                torch.uint8: PKV_FP8_E4M3, torch.float32: PKV_F32}
@@ -101,6 +104,9 @@ def load_library():
         lib.pkv_decode_step.restype = I32
         lib.pkv_decode_step.argtypes = [D, P, P, P, P, P, P, I32, P, P, I32, I32, I32,
                                         ctypes.c_float, P, I32, I32, P, SZ, P]
+        lib.pkv_paged_decode_attention_noalloc.restype = I32
+        lib.pkv_paged_decode_attention_noalloc.argtypes = [D, P, P, P, P, P, I32, I32, I32,
+                                                           ctypes.c_float, P, I32, I32, P]
         lib.pkv_kv_bytes_per_token.restype = U64
         lib.pkv_kv_bytes_per_token.argtypes = [I32, I32, I32, I32]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -225,6 +231,29 @@ def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _stream_handle(stream, q.device))
     _check(st, "pkv_decode_step")
+
+
+def pkv_paged_decode_attention_noalloc(desc: CacheDesc, q: torch.Tensor,
+                                       k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                       block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                       scale: float, out: torch.Tensor,
+                                       max_context_len_hint: int = 0, stream=None) -> None:
+    """Decode attention on the library's fixed device scratch (no workspace).
+
+    For callers that cannot allocate device memory at call time.  Calls that
+    overlap on the GPU share the scratch and race; the first call on a device
+    should come before any stream capture."""
+    lib = load_library()
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    B, mbs = int(block_tables.shape[0]), int(block_tables.shape[1])
+    st = lib.pkv_paged_decode_attention_noalloc(
+        ctypes.byref(desc), _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(context_lens, "context_lens"), B, mbs, int(max_context_len_hint),
+        float(scale), _dev_ptr(out, "out"), _DTYPE_CODE.get(q.dtype, -1),
+        _DTYPE_CODE.get(out.dtype, -1), _stream_handle(stream, q.device))
+    _check(st, "pkv_paged_decode_attention_noalloc")
 
 
 def pkv_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:

@@ -112,6 +112,18 @@ WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t 
   return w;
 }
 
+}  // namespace
+
+namespace pkv {
+// Bytes at the start of a decode workspace that must be zero when a call
+// begins (the per-segment arrival tickets).
+size_t decode_workspace_zero_bytes(const pkv_cache_desc* d, int32_t batch) {
+  return align256((size_t)batch * d->num_kv_heads * sizeof(int32_t));
+}
+}  // namespace pkv
+
+namespace {
+
 pkv_status encode_cache_map(CUtensorMap* map, const void* cache, const pkv_cache_desc* d) {
   auto fn = encode_fn();
   if (fn == nullptr) return PKV_ERR_CUDA;

@@ -88,6 +88,10 @@ inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
 cudaError_t launch_decode_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_e4m3(const DecodeLaunch& l);
+// Bytes at the start of a decode workspace that must be zero when a call
+// begins.
+size_t decode_workspace_zero_bytes(const pkv_cache_desc* d, int32_t batch);
+
 cudaError_t launch_append(const AppendParams& a, CacheKind cache, bool in_bf16,
                           cudaStream_t stream);
 
