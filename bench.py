@@ -202,10 +202,8 @@ def capture(fn, stream):
 
 def run_native(args, cfg, rank, world, device):
     stream = torch.cuda.Stream(device)
-    per_set = wl.cache_bytes_per_step(cfg, torch.tensor([0]))  # placeholder
     hint = {"llama3_8b_b32_ctx1-4096_bf16": 4096}.get(cfg.name, 0)
     # replicas: enough pool copies that the rotation spans >= 4x L2
-    w_probe_bytes = None
     with torch.cuda.stream(stream):
         probe = Step(cfg, device, 1, hint)
     pool_bytes = probe.kc[0].numel() * probe.kc[0].element_size() * 2

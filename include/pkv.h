@@ -142,6 +142,9 @@ PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t ba
  *                 256-byte aligned, zero-filled before its first use (see
  *                 pkv_decode_workspace_bytes); not shared with concurrent
  *                 calls.
+ * Results are bitwise repeatable for the same inputs, sizes and device: the
+ * work split depends only on the context lengths and the SM count, and
+ * partial sums are always added in the same order.
  * The kernel is launched as a programmatic dependent of the preceding
  * kernel on the stream but waits for it to complete before reading any
  * input, so ordinary stream order holds. */

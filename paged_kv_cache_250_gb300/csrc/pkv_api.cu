@@ -86,29 +86,28 @@ struct WsLayout {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace: per-segment arrival tickets (must start at zero; the kernel
-// returns them to zero), then the split partials, one slot per possible
-// chunk id (cta + segment).
+// Workspace: the per-segment page tickets (must start at zero; the kernel
+// returns them to zero), then ctas + segments partial slots (slot cta + seg).
 WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t hint,
                    int num_sms) {
   const int64_t g = d->num_q_heads / d->num_kv_heads;
   const int64_t cap = (int64_t)mbs * kPageSize;
   const int64_t len = (hint > 0 && hint < cap) ? hint : cap;
-  const int64_t pages_bound =
-      (int64_t)batch * d->num_kv_heads * ((len + kPageSize - 1) / kPageSize);
+  const int64_t np_max = (len + kPageSize - 1) / kPageSize;
+  const int64_t segs = (int64_t)batch * d->num_kv_heads;
+  const int64_t pages_bound = segs * np_max;
   // at least two pages per warp; at most kDecodeCtasPerSm CTAs per SM
   int64_t ctas = (pages_bound + 2 * pkv::kDecodeWarps - 1) / (2 * pkv::kDecodeWarps);
   const int64_t max_ctas = (int64_t)num_sms * pkv::kDecodeCtasPerSm;
   if (ctas > max_ctas) ctas = max_ctas;
   if (ctas < 1) ctas = 1;
-  const int64_t segs = (int64_t)batch * d->num_kv_heads;
-  const int64_t chunks = ctas + segs;
+  const int64_t slots = ctas + segs;
   WsLayout w;
   w.ctas = (int)ctas;
   w.ticket_off = 0;
-  w.ml_off = align256((size_t)segs * sizeof(int32_t));
-  w.o_off = align256(w.ml_off + (size_t)chunks * g * 2 * sizeof(float));
-  w.total = align256(w.o_off + (size_t)chunks * g * d->head_dim * sizeof(float));
+  w.ml_off = align256(w.ticket_off + (size_t)segs * sizeof(int32_t));
+  w.o_off = align256(w.ml_off + (size_t)slots * g * 2 * sizeof(float));
+  w.total = align256(w.o_off + (size_t)slots * g * d->head_dim * sizeof(float));
   return w;
 }
 
@@ -116,7 +115,7 @@ WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t 
 
 namespace pkv {
 // Bytes at the start of a decode workspace that must be zero when a call
-// begins (the per-segment arrival tickets).
+// begins (the page tickets).
 size_t decode_workspace_zero_bytes(const pkv_cache_desc* d, int32_t batch) {
   return align256((size_t)batch * d->num_kv_heads * sizeof(int32_t));
 }

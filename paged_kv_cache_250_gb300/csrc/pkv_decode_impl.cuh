@@ -12,23 +12,27 @@
 // partial outputs are brought to a common maximum by the same factor).
 //
 // Schedule.  The (sequence b, KV head h, page) units are laid out b-major,
-// then h, then page, and cut into equal contiguous ranges, one per CTA of a
-// persistent grid (two CTAs per SM).  Inside a CTA, page j of the range goes
-// to warp j % 4, so the four warps move through the same (b, h) "segment"
-// together.  When the CTA's range leaves a segment, the four warps' online-
-// softmax states are merged in shared memory.  A segment wholly inside one
-// CTA is normalised and written at once; otherwise each CTA that touches it
-// stores a partial (m, l, o) under chunk id (cta + segment), which is unique,
-// and the last CTA to finish the segment (an atomic ticket, no waiting)
-// merges the partials and writes the output.  Ragged lengths therefore never
-// leave SMs idle and no separate combine launch is needed.
+// then h, then page, and cut into equal contiguous shares, one per CTA of a
+// persistent grid (two CTAs per SM), so ragged lengths never leave an SM
+// idle.  A CTA walks its share in pieces of at most kRangeMax pages; page j
+// of a piece goes to warp j % 4, so the four warps move through the same
+// (b, h) "segment" together, each keeping its own online-softmax state.
+// When the share leaves a segment the four states are merged in shared
+// memory (the merge is order-independent).  A segment wholly inside one share
+// is normalised and written at once; a segment cut by share boundaries gets
+// one partial (m, l, o) per CTA, stored in slot cta + segment, and a
+// page-count ticket; the CTA whose pages complete the segment merges its
+// partials (the split combine), in slot order, at its next CTA barrier.
+// Nothing waits on another CTA, and every sum is taken in a fixed order, so
+// results are bitwise repeatable.
 //
 // Data path per warp.  A ring of kStages shared-memory slots, each holding
 // one K page and one V page of one (block, KV head).  Lane 0 issues 2-D TMA
 // tile loads (128-byte swizzle, evict-first L2 policy) that complete on the
 // slot's mbarrier; the warp waits, computes, and refills the slot with its
-// page kStages ahead.  Block-table lookups are done 32 pages at a time, one
-// per lane, into a small descriptor window in shared memory.
+// page kStages ahead.  Block-table lookups for a range are done by the
+// warp's lanes in parallel into a descriptor ring in shared memory, one range
+// ahead of their use.
 //
 // Math per page (16 tokens), all on warp-level tensor-core MMAs:
 //   S^T[16 tok][8] = K[16][d] . Q^T[d][8]   K via ldmatrix from the swizzled
@@ -58,6 +62,7 @@ namespace pkv {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr int kMergeBarrier = 1;                  // named barrier id (0 = __syncthreads)
+constexpr int kDescRing = 64;                     // page descriptors per warp
 
 template <int D, int CACHE>
 struct DecodeCfg {
@@ -132,14 +137,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   const int tid = threadIdx.x;
   const uint32_t ring = base + (uint32_t)(warp * kS * C::kStageBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + (size_t)NW * kS * C::kStageBytes);
-  int4* win_all = reinterpret_cast<int4*>(bars + NW * kS);
-  int4* win = win_all + warp * 64;
-  float* mbuf = reinterpret_cast<float*>(win_all + NW * 64);  // [2][kLaneState][32]
-  int* flag = reinterpret_cast<int*>(mbuf + 2 * C::kLaneState * 32);
-  int32_t* pfx = flag + 4;           // [B+1]
-  int32_t* ctxs = pfx + (p.B + 1);   // [B]
+  int2* desc_all = reinterpret_cast<int2*>(bars + NW * kS);           // [NW][kDescRing]
+  int2* desc = desc_all + warp * kDescRing;
+  float* mbuf = reinterpret_cast<float*>(desc_all + NW * kDescRing);  // [2][kLaneState][32]
+  int* flag = reinterpret_cast<int*>(mbuf + 2 * C::kLaneState * 32);  // [4]
+  int32_t* pfx = flag + 4;                                            // [B+1] pages
+  int32_t* ctxs = pfx + (p.B + 1);                                    // [B]
+  const int64_t Gn = gridDim.x;
 
-  // ---- prologue: pages per sequence and their prefix sums (whole CTA)
+  // ---- prologue: pages per sequence and their prefix sums
   if (tid == 0) pfx[0] = 0;
   for (int b = tid; b < p.B; b += blockDim.x) {
     int c = p.context_lens[b];
@@ -158,39 +164,37 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 0) {  // inclusive scan of the page counts
+    int32_t* arr = pfx;
     int carry = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int idx = b0 + lane + 1;
-      int v = (idx <= p.B) ? pfx[idx] : 0;
+      int v = (idx <= p.B) ? arr[idx] : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, off);
         if (lane >= off) v += u;
       }
-      if (idx <= p.B) pfx[idx] = v + carry;
+      if (idx <= p.B) arr[idx] = v + carry;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
   __syncthreads();
 
-  // ---- sequences with no tokens get a zero output row (spread over CTAs)
-  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-    if (pfx[b + 1] != pfx[b]) continue;
-    const int64_t row0 = (int64_t)b * p.Hq * D;
-    for (int i = tid; i < p.Hq * D; i += blockDim.x) store_out_rt(p.out_dtype, p.out, row0 + i, 0.f);
-  }
-
-  // ---- this CTA's contiguous range of the (b, h, page) units
-  const int64_t W = (int64_t)p.Hkv * pfx[p.B];
-  const int64_t Gc = W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x;  // CTAs with work
-  const int cta = blockIdx.x;
-  if (cta >= Gc) return;
-  const int64_t lo = W * cta / Gc;
-  const int64_t hi = W * (cta + 1) / Gc;
-  const int n = (int)(hi - lo);
-  const int nk = n > warp ? (n - warp + NW - 1) / NW : 0;  // pages of this warp
-  auto cta_of = [&](int64_t x) -> int64_t { return ((x + 1) * Gc - 1) / W; };
+  const int64_t W = (int64_t)p.Hkv * pfx[p.B];  // all (b, h, page) units
+  // CTA c owns the fixed share [c W / Gs, (c+1) W / Gs) of the units (Gs CTAs,
+  // each with at least about kRangeMin pages), processed in pieces of at most
+  // kRangeMax pages.  cta_of(x) is the CTA whose share holds unit x.
+  const int64_t Gs_raw = (W + kRangeMin - 1) / kRangeMin;
+  const int64_t Gs = Gs_raw < Gn ? (Gs_raw > 0 ? Gs_raw : 1) : Gn;
+  const int64_t sh_lo = blockIdx.x < Gs ? W * blockIdx.x / Gs : W;
+  const int64_t sh_hi = blockIdx.x < Gs ? W * (blockIdx.x + 1) / Gs : W;
+  auto cta_of = [&](int64_t x) -> int64_t { return ((x + 1) * Gs - 1) / W; };
+  auto piece = [&](int i) -> int2 {
+    const int64_t s0 = sh_lo + (int64_t)i * kRangeMax;
+    if (s0 >= sh_hi) return make_int2((int)W, (int)W);
+    return make_int2((int)s0, (int)(s0 + kRangeMax < sh_hi ? s0 + kRangeMax : sh_hi));
+  };
   auto seq_of = [&](int64_t x) -> int {
     int a = 0, z = p.B;
     while (z - a > 1) {
@@ -199,40 +203,94 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
     return a;
   };
+  // The warp's pages of piece [s, e) are s + warp + 4j; ordinals continue
+  // across pieces; desc[] holds 64 ordinals (two pieces of at most
+  // kRangeMax / 4 = 16 pages per warp each).
+  auto warp_count = [&](int2 r) -> int {
+    const int n = r.y - r.x - warp;
+    return n > 0 ? (n + NW - 1) / NW : 0;
+  };
+  auto fill_desc = [&](int2 r, int ord0) {  // {tma row or -1, valid tokens}
+    const int cnt = warp_count(r);
+    for (int j = lane; j < cnt; j += 32) {
+      const int64_t x = (int64_t)r.x + warp + (int64_t)NW * j;
+      const int b = seq_of(x);
+      const int np = pfx[b + 1] - pfx[b];
+      const int64_t rr = x - (int64_t)p.Hkv * pfx[b];
+      const int h = (int)(rr / np);
+      const int pg = (int)(rr - (int64_t)h * np);
+      const int blk = p.block_tables[(int64_t)b * p.MBS + pg];
+      int row = -1;
+      if (blk >= 0 && blk < p.NB) row = (blk * p.Hkv + h) * kPageSize;
+      else report_error(p.err_word, PKV_ERR_BOUNDS);
+      desc[(ord0 + j) % kDescRing] = make_int2(row, min(kPageSize, ctxs[b] - pg * kPageSize));
+      if (j == 0 || pg == 0) {  // a segment may start here: warm its q rows in L2
+        const char* qp = reinterpret_cast<const char*>(p.q) + ((int64_t)b * p.Hq + h * G) * D * 2;
+        for (int off = 0; off < G * D * 2; off += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + off));
+      }
+    }
+    __syncwarp();
+  };
+
+  // The same for the next piece, in two halves so the table loads never
+  // stall the warp: fill_issue starts the loads (one page per lane), and
+  // fill_commit, a page later, writes the descriptors.
+  int f_blk = -1, f_h = 0, f_valid = 0, f_ord = 0, f_cnt = 0;
+  bool f_pending = false;
+  auto fill_issue = [&](int2 r, int ord0) {
+    f_cnt = warp_count(r);
+    f_ord = ord0;
+    f_pending = true;
+    if (lane < f_cnt) {
+      const int64_t x = (int64_t)r.x + warp + (int64_t)NW * lane;
+      const int b = seq_of(x);
+      const int np = pfx[b + 1] - pfx[b];
+      const int64_t rr = x - (int64_t)p.Hkv * pfx[b];
+      f_h = (int)(rr / np);
+      const int pg = (int)(rr - (int64_t)f_h * np);
+      f_blk = p.block_tables[(int64_t)b * p.MBS + pg];
+      f_valid = min(kPageSize, ctxs[b] - pg * kPageSize);
+      if (lane == 0 || pg == 0) {  // a segment may start here: warm its q rows in L2
+        const char* qp = reinterpret_cast<const char*>(p.q) + ((int64_t)b * p.Hq + f_h * G) * D * 2;
+        for (int off = 0; off < G * D * 2; off += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + off));
+      }
+    }
+  };
+  auto fill_commit = [&]() -> bool {
+    if (!f_pending) return false;
+    f_pending = false;
+    if (lane < f_cnt) {
+      int row = -1;
+      if (f_blk >= 0 && f_blk < p.NB) row = (f_blk * p.Hkv + f_h) * kPageSize;
+      else report_error(p.err_word, PKV_ERR_BOUNDS);
+      desc[(f_ord + lane) % kDescRing] = make_int2(row, f_valid);
+    }
+    __syncwarp();
+    return true;
+  };
 
   if (lane == 0) {
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
   }
   const uint64_t pol = l2_policy_evict_first();
-  if (p.early_prologue) griddep_wait();  // the cache pages may have just been appended
 
-  // ---- page descriptors: {tma row or -1, segment id, page in sequence, valid tokens}
-  auto fill_window = [&](int m) {
-    const int k = 32 * m + lane;
-    int4 dsc = make_int4(-1, -1, 0, 0);
-    if (k < nk) {
-      const int64_t x = lo + warp + (int64_t)NW * k;
-      const int b = seq_of(x);
-      const int np = pfx[b + 1] - pfx[b];
-      const int64_t r = x - (int64_t)p.Hkv * pfx[b];
-      const int h = (int)(r / np);
-      const int pg = (int)(r - (int64_t)h * np);
-      const int blk = p.block_tables[(int64_t)b * p.MBS + pg];
-      int row = -1;
-      if (blk >= 0 && blk < p.NB) row = (blk * p.Hkv + h) * kPageSize;
-      else report_error(p.err_word, PKV_ERR_BOUNDS);
-      dsc = make_int4(row, b * p.Hkv + h, pg, min(kPageSize, ctxs[b] - pg * kPageSize));
-    }
-    win[(m & 1) * 32 + lane] = dsc;
-    __syncwarp();
-  };
+  // the first two pieces and their descriptors need nothing the previous
+  // kernel writes (lengths and tables only)
+  const int2 r0 = piece(0), r1 = piece(1);
+  fill_desc(r0, 0);
+  fill_desc(r1, warp_count(r0));
 
-  int issued = 0;
+  // From here on the kernel touches data the previous kernel on the stream may
+  // write (cache pages, q, outputs, workspace): wait for it.
+  if (p.early_prologue) griddep_wait();
+
+  int issued = 0;      // ordinals whose load was issued
+  int filled_end = 0;  // ordinals with a descriptor
   auto issue = [&](int i) {
-    issued = i + 1;
-    if ((i & 31) == 0) fill_window(i >> 5);
-    const int4 dsc = win[((i >> 5) & 1) * 32 + (i & 31)];
+    const int2 dsc = desc[i % kDescRing];
     if (lane == 0) {
       const int slot = i % kS;
       const uint32_t bar = smem_u32(&bars[warp * kS + slot]);
@@ -250,6 +308,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       }
     }
   };
+  auto top_up = [&](int consumed) {  // keep kS loads in flight
+    while (issued < consumed + kS && issued < filled_end) issue(issued++);
+  };
+  filled_end = warp_count(r0) + warp_count(r1);
+  top_up(0);
+
+  // sequences with no tokens get a zero output row (spread over CTAs)
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    if (pfx[b + 1] != pfx[b]) continue;
+    const int64_t row0 = (int64_t)b * p.Hq * D;
+    for (int i = tid; i < p.Hq * D; i += blockDim.x) store_out_rt(p.out_dtype, p.out, row0 + i, 0.f);
+  }
 
   // ---- per-lane fragment coordinates
   const int c4 = lane & 3;   // C-fragment column pair: heads 2*c4, 2*c4+1
@@ -318,12 +388,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     // ---- S^T = K . Q^T
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     if constexpr (CACHE != kCacheE4M3) {
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: halves the MMA chain
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
         uint32_t a[4];
         ldsm_x4(a, kt + swz(qk_tok, 2 * ks + qk_chunk_hi));
-        mma_16816<kBF>(s, a, qf[ks][0], qf[ks][1]);
+        if (ks & 1) mma_16816<kBF>(s2, a, qf[ks][0], qf[ks][1]);
+        else mma_16816<kBF>(s, a, qf[ks][0], qf[ks][1]);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[e] += s2[e];
     } else {
 #pragma unroll
       for (int gi = 0; gi < D / 32; ++gi) {
@@ -460,198 +534,287 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         o[mt][e] = a[e & 1] * o[mt][e] + bw[e & 1] * buf[(4 + 4 * mt + e) * 32 + lane];
   };
 
-  // ---- end of a segment: merge the 4 warps, then write output or a partial
-  auto end_segment = [&](int b, int h, int64_t seg_start, int64_t seg_end) {
-    const int seg = b * p.Hkv + h;
+  // ---- merging the partials of a segment this CTA completed (all threads).
+  // Pass 1: the common maximum M per query head, all threads over all
+  // partials.  Pass 2: warp w takes partials w, w+4, ...; lane c takes float4
+  // columns c, c+32, ...; weighted sums with independent loads; then the four
+  // warps' sums are added in shared memory and the output written.
+  auto merge_segment = [&](int seg) {
+    // the partials of CTAs cta_of(first unit) .. cta_of(last unit), stored
+    // under slots cta + seg
+    const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+    const int64_t np = pfx[b + 1] - pfx[b];
+    const int64_t s0 = (int64_t)p.Hkv * pfx[b] + (int64_t)h * np;
+    const int64_t c0 = cta_of(s0);
+    const int count = (int)(cta_of(s0 + np - 1) - c0 + 1);
+    const int64_t slot_base = c0 + seg;
+    constexpr int kCols = G * D / 4;        // float4 columns of the output
+    constexpr int kCPL = (kCols + 31) / 32;  // columns per lane
+    // shared buffers (inside the 2 * kLaneState * 32 floats of mbuf):
+    // Mh [NW][8] maxima, Lr [NW][8] sums, red [NW][kHalf] float4 warp sums
+    constexpr int kBudget = (2 * C::kLaneState * 32 - 2 * NW * 8) / (4 * NW);
+    constexpr int kHalf = kCols < (kBudget & ~31) ? kCols : (kBudget & ~31);
+    static_assert(kHalf >= (kCols < 32 ? kCols : 32), "merge buffer too small");
+    float* Mh = mbuf;
+    float* Lr = mbuf + NW * 8;
+    float4* red = reinterpret_cast<float4*>(mbuf + 2 * NW * 8);
+    // pass 1
+    float mloc = -INFINITY;
+    for (int i = tid; i < count * G; i += NW * 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot_base * G + i) * 2));
+      if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
+    }
+    for (int off = G; off < 32; off <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+    if (lane < G) Mh[warp * 8 + lane] = mloc;
+    merge_barrier();
+    // pass 2, kHalf columns per round (a head's columns never straddle two
+    // rounds: D / 4 divides kHalf)
+    constexpr int kCPR = (kHalf + 31) / 32;  // columns per lane per round
+    static_assert(kHalf % (D / 4) == 0 || kHalf == kCols, "head split across rounds");
+#pragma unroll 1
+    for (int r0 = 0; r0 < kCols; r0 += kHalf) {
+      float4 acc[kCPR];
+      float lsum[kCPR];
+      float Mc[kCPR];
+#pragma unroll
+      for (int j = 0; j < kCPR; ++j) {
+        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        lsum[j] = 0.f;
+        const int col = r0 + lane + 32 * j;
+        const int head = (col < kCols ? col : 0) / (D / 4);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, Mh[w * 8 + head]);
+        Mc[j] = M;
+      }
+#pragma unroll 2
+      for (int kk = warp; kk < count; kk += NW) {
+        const int64_t part = slot_base + kk;
+#pragma unroll
+        for (int j = 0; j < kCPR; ++j) {
+          const int col = r0 + lane + 32 * j;
+          if (lane + 32 * j < kHalf && col < kCols) {
+            const int head = col / (D / 4);
+            const float2 ml =
+                __ldcg(reinterpret_cast<const float2*>(p.part_ml + (part * G + head) * 2));
+            const float4 v =
+                __ldcg(reinterpret_cast<const float4*>(p.part_o + part * G * D) + col);
+            const float w = (ml.y > 0.f && Mc[j] > -INFINITY) ? exp2f(ml.x - Mc[j]) : 0.f;
+            lsum[j] += w * ml.y;
+            acc[j].x += w * v.x;
+            acc[j].y += w * v.y;
+            acc[j].z += w * v.z;
+            acc[j].w += w * v.w;
+          }
+        }
+      }
+      // add the warps' sums; a head's l is the same in every lane holding one
+      // of its columns
+      if (r0 > 0) merge_barrier();  // the previous round's readers are done
+#pragma unroll
+      for (int j = 0; j < kCPR; ++j) {
+        const int c = lane + 32 * j;
+        const int col = r0 + c;
+        if (c < kHalf && col < kCols) {
+          red[warp * kHalf + c] = acc[j];
+          if (col % (D / 4) == 0) Lr[warp * 8 + col / (D / 4)] = lsum[j];
+        }
+      }
+      merge_barrier();
+      for (int c = tid; c < kHalf && r0 + c < kCols; c += NW * 32) {
+        const int col = r0 + c;
+        const int head = col / (D / 4);
+        float4 t = red[c];
+        float L = Lr[head];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+          const float4 v = red[w * kHalf + c];
+          t.x += v.x;
+          t.y += v.y;
+          t.z += v.z;
+          t.w += v.w;
+          L += Lr[w * 8 + head];
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
+        store_out_rt(p.out_dtype, p.out, ob + 0, t.x * inv);
+        store_out_rt(p.out_dtype, p.out, ob + 1, t.y * inv);
+        store_out_rt(p.out_dtype, p.out, ob + 2, t.z * inv);
+        store_out_rt(p.out_dtype, p.out, ob + 3, t.w * inv);
+      }
+    }
+    if (tid == 0) p.tickets[seg] = 0;  // ready for the next call
+  };
+
+  // A CTA learns it completed a split segment from the page-count ticket it
+  // added with a release atomic when it stored its partial.  Thread 0 checks
+  // the returned count only before the CTA's next barrier, so the atomic never
+  // stalls the stream; the merge then runs right after that barrier.
+  int pend_seg = -1, tk_old = 0, tk_add = 0, tk_np = 0;  // thread 0
+  auto resolve_ticket = [&]() {  // thread 0, before a CTA barrier
+    if (pend_seg >= 0) {
+      if (tk_old + tk_add == tk_np) {
+        __threadfence();  // acquire: the other contributors' partials
+        flag[1] = pend_seg;
+      }
+      pend_seg = -1;
+    }
+  };
+  auto merge_if_flagged = [&]() {  // all threads, right after a CTA barrier
+    const int seg = flag[1];
+    if (seg >= 0) {
+      __threadfence();
+      merge_segment(seg);
+      merge_barrier();
+      if (tid == 0) flag[1] = -1;
+    }
+  };
+
+  // ---- end of this CTA's part of a segment: merge the 4 warps' states, then
+  // write the output (whole segment here) or this CTA's partial and ticket
+  auto flush = [&](int b, int h, bool split, int pages_mine) {
     float* buf0 = mbuf;
     float* buf1 = mbuf + C::kLaneState * 32;
+    if (tid == 0) resolve_ticket();
+    merge_barrier();
+    merge_if_flagged();  // uses mbuf, before the states go there
     if (warp >= 2) store_state(warp == 2 ? buf0 : buf1);
     merge_barrier();
     if (warp < 2) merge_state(warp == 0 ? buf0 : buf1);
     merge_barrier();
     if (warp == 1) store_state(buf0);
     merge_barrier();
+    if (warp != 0) return;
+    merge_state(buf0);
     const float vs = (CACHE == kCacheE4M3) ? p.v_scale[h] : 1.f;
-    const int64_t c_first = cta_of(seg_start);
-    const int64_t count = cta_of(seg_end - 1) - c_first + 1;
     const int h0 = 2 * c4, h1 = 2 * c4 + 1;
-    if (warp == 0) {
-      merge_state(buf0);
-      float lt0 = l2[0], lt1 = l2[1];
+    float lt0 = l2[0], lt1 = l2[1];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
-        lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+    for (int off = 4; off < 32; off <<= 1) {
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+    }
+    if (!split) {  // the whole segment was here: normalise and write
+      const float i0 = lt0 > 0.f ? vs / lt0 : 0.f;
+      const float i1 = lt1 > 0.f ? vs / lt1 : 0.f;
+      const int64_t ob = ((int64_t)b * p.Hq + h * G) * D;
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int dA = d_of(mt, 0), dB = d_of(mt, 1);
+        if (h0 < G) {
+          store_out_rt(p.out_dtype, p.out, ob + h0 * D + dA, o[mt][0] * i0);
+          store_out_rt(p.out_dtype, p.out, ob + h0 * D + dB, o[mt][2] * i0);
+        }
+        if (h1 < G) {
+          store_out_rt(p.out_dtype, p.out, ob + h1 * D + dA, o[mt][1] * i1);
+          store_out_rt(p.out_dtype, p.out, ob + h1 * D + dB, o[mt][3] * i1);
+        }
       }
-      if (count == 1) {
-        // the whole segment is here: normalise and write the output rows
-        const float i0 = lt0 > 0.f ? vs / lt0 : 0.f;
-        const float i1 = lt1 > 0.f ? vs / lt1 : 0.f;
-        const int64_t ob = ((int64_t)b * p.Hq + h * G) * D;
+      return;
+    }
+    // partial slot cta + seg is unique: shares are contiguous and ordered, so
+    // a later CTA never touches an earlier segment
+    const int64_t part = (int64_t)blockIdx.x + b * p.Hkv + h;
+    float* po = p.part_o + part * G * D;
+    float* pml = p.part_ml + part * G * 2;
+    if (r8 == 0) {
+      if (h0 < G) { pml[2 * h0] = m2[0]; pml[2 * h0 + 1] = lt0; }
+      if (h1 < G) { pml[2 * h1] = m2[1]; pml[2 * h1 + 1] = lt1; }
+    }
 #pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          const int dA = d_of(mt, 0), dB = d_of(mt, 1);
-          if (h0 < G) {
-            store_out_rt(p.out_dtype, p.out, ob + h0 * D + dA, o[mt][0] * i0);
-            store_out_rt(p.out_dtype, p.out, ob + h0 * D + dB, o[mt][2] * i0);
-          }
-          if (h1 < G) {
-            store_out_rt(p.out_dtype, p.out, ob + h1 * D + dA, o[mt][1] * i1);
-            store_out_rt(p.out_dtype, p.out, ob + h1 * D + dB, o[mt][3] * i1);
-          }
-        }
-      } else {
-        const int64_t chunk = (int64_t)cta + seg;
-        float* po = p.part_o + chunk * G * D;
-        float* pml = p.part_ml + chunk * G * 2;
-        if (r8 == 0) {
-          if (h0 < G) { pml[2 * h0] = m2[0]; pml[2 * h0 + 1] = lt0; }
-          if (h1 < G) { pml[2 * h1] = m2[1]; pml[2 * h1 + 1] = lt1; }
-        }
-#pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          const int dA = d_of(mt, 0), dB = d_of(mt, 1);
-          if (h0 < G) {
-            po[h0 * D + dA] = o[mt][0] * vs;
-            po[h0 * D + dB] = o[mt][2] * vs;
-          }
-          if (h1 < G) {
-            po[h1 * D + dA] = o[mt][1] * vs;
-            po[h1 * D + dB] = o[mt][3] * vs;
-          }
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) {
-          const int old = atomicAdd(&p.tickets[seg], 1);
-          flag[0] = (old == count - 1) ? 1 : 0;
-        }
+    for (int mt = 0; mt < kMT; ++mt) {
+      const int dA = d_of(mt, 0), dB = d_of(mt, 1);
+      if (h0 < G) {
+        po[h0 * D + dA] = o[mt][0] * vs;
+        po[h0 * D + dB] = o[mt][2] * vs;
+      }
+      if (h1 < G) {
+        po[h1 * D + dA] = o[mt][1] * vs;
+        po[h1 * D + dB] = o[mt][3] * vs;
       }
     }
-    merge_barrier();
-    if (count > 1 && flag[0]) {
-      // last CTA of this segment: merge every chunk's partial (all threads)
-      __threadfence();
-      const int64_t first = c_first + seg;
-      constexpr int kCols = G * D / 4;  // float4 columns of the segment's output
-      constexpr int kThreads = NW * 32;
-      constexpr int kPerPass = kCols < kThreads ? kCols : kThreads;
-      constexpr int kGroups = kThreads / kPerPass;  // chunk subsets merged in parallel
-      float4* red = reinterpret_cast<float4*>(mbuf);      // [kGroups][kCols]
-      float* lred = mbuf + 4 * kGroups * kCols;           // [kGroups][G]
-      float* Ms = lred + kGroups * G;                     // [G]
-      if (tid < G) {
-        float M = -INFINITY;
-        for (int64_t kk = 0; kk < count; ++kk) {
-          const float2 ml = __ldcg(
-              reinterpret_cast<const float2*>(p.part_ml + ((first + kk) * G + tid) * 2));
-          if (ml.y > 0.f) M = fmaxf(M, ml.x);
-        }
-        Ms[tid] = M;
-      }
-      merge_barrier();
-      const int grp = tid / kPerPass;
-      for (int col = tid % kPerPass; col < kCols; col += kPerPass) {
-        const int head = col / (D / 4);
-        const float M = Ms[head];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lsum = 0.f;
-        if (M > -INFINITY) {
-#pragma unroll 4
-          for (int64_t kk = grp; kk < count; kk += kGroups) {
-            const float2 ml = __ldcg(
-                reinterpret_cast<const float2*>(p.part_ml + ((first + kk) * G + head) * 2));
-            if (!(ml.y > 0.f)) continue;
-            const float w = exp2f(ml.x - M);
-            lsum += w * ml.y;
-            const float4 v =
-                __ldcg(reinterpret_cast<const float4*>(p.part_o + (first + kk) * G * D) + col);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-          }
-        }
-        if constexpr (kGroups == 1) {
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-          const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
-          store_out_rt(p.out_dtype, p.out, ob + 0, acc.x * inv);
-          store_out_rt(p.out_dtype, p.out, ob + 1, acc.y * inv);
-          store_out_rt(p.out_dtype, p.out, ob + 2, acc.z * inv);
-          store_out_rt(p.out_dtype, p.out, ob + 3, acc.w * inv);
-        } else {
-          red[grp * kCols + col] = acc;
-          if ((col % (D / 4)) == 0) lred[grp * G + head] = lsum;
-        }
-      }
-      if constexpr (kGroups > 1) {
-        merge_barrier();
-        if (tid < kCols) {
-          const int col = tid;
-          const int head = col / (D / 4);
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          float L = 0.f;
-#pragma unroll
-          for (int g2 = 0; g2 < kGroups; ++g2) {
-            const float4 v = red[g2 * kCols + col];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-            L += lred[g2 * G + head];
-          }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
-          store_out_rt(p.out_dtype, p.out, ob + 0, acc.x * inv);
-          store_out_rt(p.out_dtype, p.out, ob + 1, acc.y * inv);
-          store_out_rt(p.out_dtype, p.out, ob + 2, acc.z * inv);
-          store_out_rt(p.out_dtype, p.out, ob + 3, acc.w * inv);
-        }
-      }
-      if (tid == 0) p.tickets[seg] = 0;  // ready for the next call
+    __syncwarp();
+    if (lane == 0) {  // publish this partial's pages; the result is read later
+      const int seg = b * p.Hkv + h;
+      int old;
+      asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;"
+                   : "=r"(old) : "l"(&p.tickets[seg]), "r"(pages_mine) : "memory");
+      pend_seg = seg;
+      tk_old = old;
+      tk_add = pages_mine;
+      tk_np = pfx[b + 1] - pfx[b];
     }
-    merge_barrier();  // buffers and flag free again
   };
 
-  // ---- main loop: segments of this CTA's range in order
-  const int pre = nk < kS ? nk : kS;
-  for (int i = 0; i < pre; ++i) issue(i);
+  // ---- main loop over the pieces of this CTA's share
   bool dead = false;  // a bounded wait gave up: skip compute, keep the barriers
   int k_dead = -1;
-  int k = 0;
-  int64_t x = lo;
-  while (true) {
-    const int b = seq_of(x);
-    const int np = pfx[b + 1] - pfx[b];
-    const int64_t sb = (int64_t)p.Hkv * pfx[b];
-    const int h = (int)((x - sb) / np);
-    const int64_t seg_start = sb + (int64_t)h * np;
-    const int64_t seg_end = seg_start + np;
-    reset_state();
-    bool have_q = false;
-    while (k < nk && lo + warp + (int64_t)NW * k < seg_end) {
-      if (!have_q) {
-        load_q(b, h);
-        have_q = true;
+  int k = 0;          // next ordinal to consume
+  int ord_base = 0;   // first ordinal of the current piece (this warp)
+  int cur_b = -1, cur_h = -1, pages_mine = 0;
+  bool split = false;  // the current segment is shared with other CTAs
+  bool have_q = false;
+  if (tid == 0) flag[1] = -1;
+  for (int n = 0;; ++n) {
+    const int2 R = (n == 0) ? r0 : piece(n);
+    if (R.x >= R.y) break;  // no more work (later pieces are empty too)
+    if (n >= 1) fill_issue(piece(n + 1), ord_base + warp_count(R));
+    // the (b, h) segments inside piece R, in order
+    int64_t x = R.x;
+    while (x < R.y) {
+      const int b = seq_of(x);
+      const int np = pfx[b + 1] - pfx[b];
+      const int64_t sb = (int64_t)p.Hkv * pfx[b];
+      const int h = (int)((x - sb) / np);
+      const int64_t seg_start = sb + (int64_t)h * np;
+      const int64_t seg_end = seg_start + np;
+      const int64_t pe = seg_end < R.y ? seg_end : R.y;
+      if (b != cur_b || h != cur_h) {
+        if (cur_b >= 0) flush(cur_b, cur_h, split, pages_mine);
+        cur_b = b;
+        cur_h = h;
+        pages_mine = 0;
+        have_q = false;
+        reset_state();
+        split = x > seg_start || seg_end > sh_hi;
       }
-      const int4 dsc = win[((k >> 5) & 1) * 32 + (k & 31)];
-      const int slot = k % kS;
-      if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + slot]),
-                                      (uint32_t)((k / kS) & 1), kWaitLimitNs)) {
-        dead = true;
-        k_dead = k;
-        if (lane == 0) report_error(p.err_word, PKV_ERR_TIMEOUT);
+      // this warp's ordinals inside [x, pe)
+      const int64_t lo_j = x - R.x - warp + NW - 1;
+      const int64_t hi_j = pe - R.x - warp + NW - 1;
+      const int j0 = (int)((lo_j > 0 ? lo_j : 0) / NW);
+      const int j1 = (int)((hi_j > 0 ? hi_j : 0) / NW);
+      for (int j = j0; j < j1; ++j, ++k) {
+        if (!have_q) {
+          load_q(b, h);
+          have_q = true;
+        }
+        const int2 dsc = desc[k % kDescRing];
+        const int slot = k % kS;
+        if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + slot]),
+                                        (uint32_t)((k / kS) & 1), kWaitLimitNs)) {
+          dead = true;
+          k_dead = k;
+          if (lane == 0) report_error(p.err_word, PKV_ERR_TIMEOUT);
+        }
+        if (!dead && dsc.x >= 0 && dsc.y > 0)
+          compute_page(ring + (uint32_t)(slot * C::kStageBytes), dsc.y);
+        __syncwarp();
+        if (fill_commit()) filled_end = f_ord + f_cnt;
+        if (!dead) top_up(k + 1);
       }
-      if (!dead && dsc.x >= 0 && dsc.w > 0)
-        compute_page(ring + (uint32_t)(slot * C::kStageBytes), dsc.w);
-      __syncwarp();
-      if (!dead && k + kS < nk) issue(k + kS);
-      ++k;
+      pages_mine += (int)(pe - x);
+      x = pe;
     }
-    end_segment(b, h, seg_start, seg_end);
-    x = seg_end;
-    if (x >= hi) break;
+    if (fill_commit()) {  // this warp had no page left in piece R
+      filled_end = f_ord + f_cnt;
+      if (!dead) top_up(k);
+    }
+    ord_base += warp_count(R);
   }
+  if (cur_b >= 0) flush(cur_b, cur_h, split, pages_mine);
+  if (tid == 0) resolve_ticket();
+  merge_barrier();
+  merge_if_flagged();
   if (dead) {
     // let the copies this warp still has in flight land (bounded) before exit
     for (int q = k_dead + 1; q < issued; ++q)

@@ -16,21 +16,28 @@ constexpr int kDecodeCtasPerSm = 2;
 
 enum CacheKind { kCacheF16 = 0, kCacheBF16 = 1, kCacheE4M3 = 2 };
 
+// A CTA's share holds at least about kRangeMin pages (fewer CTAs run when
+// the batch is small) and is walked in pieces of at most kRangeMax pages.
+constexpr int kRangeMin = 8;
+constexpr int kRangeMax = 64;
+
 // Shared-memory plan of the decode kernel (host and device agree on it).
 constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
 constexpr int decode_stage_bytes(int d, CacheKind c) {
   return 2 * kPageSize * d * (c == kCacheE4M3 ? 1 : 2);
 }
-// alignment slack + descriptor windows + merge buffers + flag + mbarriers (8 max)
+// alignment slack + descriptor rings + merge buffers + flags + mbarriers (8 max)
 constexpr int decode_fixed_smem(int d) {
-  return 1024 + kDecodeWarps * 64 * 16 + 2 * decode_lane_state(d) * 32 * 4 + 16 +
+  return 1024 + kDecodeWarps * 64 * 8 + 2 * decode_lane_state(d) * 32 * 4 + 16 +
          kDecodeWarps * 8 * 8;
 }
-// Ring depth: as many K+V page slots per warp as fit two CTAs per SM with
-// room for a 256-sequence prefix array; between 2 and 8.
+// Ring depth: as many K+V page slots per warp as fit two CTAs per SM (228 KB
+// per SM, 1 KB reserved per CTA) with room for the per-sequence arrays of a
+// 128-sequence batch; between 2 and 8.
+constexpr int kDecodeSmemTarget = 113 * 1024;
 constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
 constexpr int decode_stages(int d, CacheKind c) {
-  return decode_clamp_stages((112 * 1024 - decode_fixed_smem(d) - 2 * 1024) /
+  return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d) - 1560) /
                              (kDecodeWarps * decode_stage_bytes(d, c)));
 }
 
@@ -41,9 +48,9 @@ struct DecodeParams {
   const int32_t* block_tables; // [B][MBS]
   const int32_t* context_lens; // [B]
   void* out;                   // [B][Hq][d]
-  float* part_o;               // [chunks][G][d]   unnormalised partial outputs
-  float* part_ml;              // [chunks][G][2]   (reference max in log2 units, sum)
-  int32_t* tickets;            // [B*Hkv]          arrivals per segment; zero between calls
+  float* part_o;               // [ctas+B*Hkv][G][d] unnormalised partial outputs
+  float* part_ml;              // [ctas+B*Hkv][G][2] (reference max in log2 units, sum)
+  int32_t* tickets;            // [B*Hkv]            pages stored per segment; zero between calls
   const float* k_scale;        // FP8 only
   const float* v_scale;        // FP8 only
   int32_t* err_word;

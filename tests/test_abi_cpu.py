@@ -5,6 +5,7 @@ import ctypes
 import json
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -34,10 +35,21 @@ def test_library_builds_and_exports_every_declared_symbol():
         pass
 
 
-def test_struct_layout_matches_header():
-    # uint32 + 5 int32 + enum (4 bytes) = 28, padded to 32, then 3 pointers
-    assert ctypes.sizeof(pkv.CacheDesc) == 56
-    assert pkv.CacheDesc.k_scale.offset == 32
+def test_struct_layout_matches_header(tmp_path):
+    # compile a tiny C program against include/pkv.h and compare every field
+    # offset and the size with the ctypes mirror
+    fields = [f[0] for f in pkv.CacheDesc._fields_]
+    src = tmp_path / "probe.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "pkv.h"\nint main(void){\n'
+                   + "".join(f'printf("%zu\\n", offsetof(pkv_cache_desc, {f}));\n' for f in fields)
+                   + 'printf("%zu\\n", sizeof(pkv_cache_desc)); return 0; }\n')
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [getattr(pkv.CacheDesc, f).offset for f in fields] + [ctypes.sizeof(pkv.CacheDesc)]
+    assert got == want
 
 
 def test_host_helpers():

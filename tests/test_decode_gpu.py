@@ -157,6 +157,8 @@ def test_append_skips_negative_slots_and_reports_out_of_pool():
 
 # ----------------------------------------------------------------- invariants
 def test_paging_is_invisible_to_the_result():
+    # work is cut into shares of logical pages, so the result is bitwise
+    # independent of where the pages sit in the pool
     ctx = torch.tensor([40, 300, 17, 1, 129])
     outs = []
     for table in ("identity", "permuted"):
@@ -171,18 +173,29 @@ def test_paging_is_invisible_to_the_result():
 
 def test_repeatable_and_zero_context_rows():
     cfg = wl.small_config("zero", 5, 8, 2, 128, "bf16", 1, seed=4)
-    w = wl.generate(cfg, ctx_override=torch.tensor([0, 33, 0, 1, 500]))
+    w = wl.generate(cfg, ctx_override=torch.tensor([0, 33, 0, 1, 5000]))
     run = GpuRun(w)
     run.append()
     a = run.decode("f32").cpu()
     b = run.decode("f32").cpu()
-    assert torch.equal(a, b)
+    assert torch.equal(a, b)  # split partials are merged in a fixed order
     assert torch.all(a[0] == 0) and torch.all(a[2] == 0)
     ref = oracle_all(w)
     assert_close(a.double().numpy(), ref, cfg, "f32", "zero-ctx batch")
     allzero = wl.generate(cfg, ctx_override=torch.tensor([0, 0, 0, 0, 0]))
     run0 = GpuRun(allzero)
     assert torch.all(run0.decode("bf16") == 0)
+
+
+def test_long_ragged_batch_is_repeatable_and_matches_the_oracle():
+    cfg = wl.small_config("det", 7, 32, 8, 128, "bf16", (1, 6000), seed=17)
+    w = wl.generate(cfg)
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    out2 = run.decode("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert np.array_equal(out, out2)
+    assert_close(out, oracle_all(w), cfg, "f32", "long ragged batch")
 
 
 def test_prefix_sharing_tables():
