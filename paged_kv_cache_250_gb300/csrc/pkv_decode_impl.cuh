@@ -12,9 +12,9 @@
 // partial outputs are brought to a common maximum by the same factor).
 //
 // Schedule.  The (sequence b, KV head h, page) units are laid out b-major,
-// then h, then page, and cut into equal contiguous shares, one per CTA of a
-// persistent grid (two CTAs per SM), so ragged lengths never leave an SM
-// idle.  A CTA walks its share in pieces of at most kRangeMax pages; page j
+// then h, then page, and cut into contiguous shares of equal cost, one per
+// CTA of a persistent grid (two CTAs per SM), so ragged lengths never leave
+// an SM idle; a page costs 1 and a segment start a few pages more.  A CTA walks its share in pieces of at most kRangeMax pages; page j
 // of a piece goes to warp j % 4, so the four warps move through the same
 // (b, h) "segment" together, each keeping its own online-softmax state.
 // When the share leaves a segment the four states are merged in shared
@@ -137,16 +137,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   const int tid = threadIdx.x;
   const uint32_t ring = base + (uint32_t)(warp * kS * C::kStageBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + (size_t)NW * kS * C::kStageBytes);
-  int2* desc_all = reinterpret_cast<int2*>(bars + NW * kS);           // [NW][kDescRing]
+  uint64_t* fbar = bars + NW * kS;  // [4] flush: full (even, odd), empty, padding
+  // everything after the mbarriers stays 16-byte aligned (float4 in mbuf)
+  static_assert((NW * kS * 8) % 16 == 0 && (NW * kDescRing * 8) % 16 == 0, "smem alignment");
+  int2* desc_all = reinterpret_cast<int2*>(fbar + 4);    // [NW][kDescRing]
   int2* desc = desc_all + warp * kDescRing;
   float* mbuf = reinterpret_cast<float*>(desc_all + NW * kDescRing);  // [2][kLaneState][32]
-  int* flag = reinterpret_cast<int*>(mbuf + 2 * C::kLaneState * 32);  // [4]
-  int32_t* pfx = flag + 4;                                            // [B+1] pages
-  int32_t* ctxs = pfx + (p.B + 1);                                    // [B]
+  int* mflag = reinterpret_cast<int*>(mbuf + 2 * C::kLaneState * 32);  // [2 NW] merges due
+  int32_t* pfx = mflag + 2 * NW;                                      // [B+1] pages
+  int32_t* nzp = pfx + (p.B + 1);                                     // [B+1] non-empty seqs
+  int32_t* ctxs = nzp + (p.B + 1);                                    // [B]
   const int64_t Gn = gridDim.x;
 
-  // ---- prologue: pages per sequence and their prefix sums
-  if (tid == 0) pfx[0] = 0;
+  // ---- prologue: pages per sequence, prefix sums of pages and of non-empty
+  // sequences
+  if (tid == 0) {
+    pfx[0] = 0;
+    nzp[0] = 0;
+  }
   for (int b = tid; b < p.B; b += blockDim.x) {
     int c = p.context_lens[b];
     int np = 0;
@@ -158,14 +166,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
     ctxs[b] = c;
     pfx[b + 1] = np;
+    nzp[b + 1] = np > 0 ? 1 : 0;
   }
   if (lane == 0) {
     for (int s = 0; s < kS; ++s) mbar_init(smem_u32(&bars[warp * kS + s]), 1);
+    if (warp == 0) {
+      mbar_init(smem_u32(fbar + 0), (NW - 1) * 32);
+      mbar_init(smem_u32(fbar + 1), (NW - 1) * 32);
+      mbar_init(smem_u32(fbar + 2), 32);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp == 0) {  // inclusive scan of the page counts
-    int32_t* arr = pfx;
+  if (warp < 2) {  // inclusive scans: warp 0 pages, warp 1 non-empty sequences
+    int32_t* arr = warp == 0 ? pfx : nzp;
     int carry = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int idx = b0 + lane + 1;
@@ -182,14 +196,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   __syncthreads();
 
   const int64_t W = (int64_t)p.Hkv * pfx[p.B];  // all (b, h, page) units
-  // CTA c owns the fixed share [c W / Gs, (c+1) W / Gs) of the units (Gs CTAs,
-  // each with at least about kRangeMin pages), processed in pieces of at most
-  // kRangeMax pages.  cta_of(x) is the CTA whose share holds unit x.
-  const int64_t Gs_raw = (W + kRangeMin - 1) / kRangeMin;
+  // Shares are equal in cost, not in pages: a page costs 1 and the start of a
+  // segment kSegCost more (the state merge, output write and pipeline refill
+  // a segment change takes), so CTAs whose share holds many short segments
+  // get fewer pages.  Unit x of segment (b, h) costs from
+  //   X(x) = Hkv (pfx[b] + kSegCost nzp[b]) + h (np_b + kSegCost) + kSegCost + (x - start)
+  // and CTA c owns the units with c T / Gs <= X(x) < (c+1) T / Gs, T the total
+  // cost, Gs the CTAs given work (each about kRangeMin pages or more).
+  const int64_t Tc = W + (int64_t)p.Hkv * kSegCost * nzp[p.B];
+  const int64_t Gs_raw = (Tc + kRangeMin - 1) / kRangeMin;
   const int64_t Gs = Gs_raw < Gn ? (Gs_raw > 0 ? Gs_raw : 1) : Gn;
-  const int64_t sh_lo = blockIdx.x < Gs ? W * blockIdx.x / Gs : W;
-  const int64_t sh_hi = blockIdx.x < Gs ? W * (blockIdx.x + 1) / Gs : W;
-  auto cta_of = [&](int64_t x) -> int64_t { return ((x + 1) * Gs - 1) / W; };
+  auto seq_cost0 = [&](int b) -> int64_t {
+    return (int64_t)p.Hkv * (pfx[b] + (int64_t)kSegCost * nzp[b]);
+  };
+  // first unit whose cost position is >= P (W when none)
+  auto unit_at_cost = [&](int64_t P) -> int64_t {
+    if (P >= Tc) return W;
+    int a = 0, z = p.B;
+    while (z - a > 1) {
+      const int mid = (a + z) >> 1;
+      if (seq_cost0(mid) <= P) a = mid; else z = mid;
+    }
+    const int64_t np = pfx[a + 1] - pfx[a];
+    const int64_t r = P - seq_cost0(a);
+    const int64_t hh = r / (np + kSegCost);
+    const int64_t off = r - hh * (np + kSegCost) - kSegCost;
+    return (int64_t)p.Hkv * pfx[a] + hh * np + (off > 0 ? off : 0);
+  };
+  const int64_t sh_lo = blockIdx.x < Gs ? unit_at_cost((Tc * blockIdx.x + Gs - 1) / Gs) : W;
+  const int64_t sh_hi = blockIdx.x < Gs ? unit_at_cost((Tc * (blockIdx.x + 1) + Gs - 1) / Gs) : W;
+  // the CTA whose share holds unit x of sequence b, KV head h
+  auto cta_of = [&](int64_t x, int b, int64_t h) -> int64_t {
+    const int64_t np = pfx[b + 1] - pfx[b];
+    const int64_t start = (int64_t)p.Hkv * pfx[b] + h * np;
+    const int64_t X = seq_cost0(b) + h * (np + kSegCost) + kSegCost + (x - start);
+    return X * Gs / Tc;
+  };
   auto piece = [&](int i) -> int2 {
     const int64_t s0 = sh_lo + (int64_t)i * kRangeMax;
     if (s0 >= sh_hi) return make_int2((int)W, (int)W);
@@ -500,22 +542,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
   };
 
-  // ---- merging warp states through shared memory (per-lane layout)
-  auto store_state = [&](float* buf) {
-    buf[0 * 32 + lane] = m2[0];
-    buf[1 * 32 + lane] = m2[1];
-    buf[2 * 32 + lane] = l2[0];
-    buf[3 * 32 + lane] = l2[1];
+  // ---- merging warp states through shared memory: element i of the lane
+  // state (m[2], l[2], o[MT][4]) at buf[i * S + li]
+  auto store_state_at = [&](float* buf, int li, int S) {
+    buf[0 * S + li] = m2[0];
+    buf[1 * S + li] = m2[1];
+    buf[2 * S + li] = l2[0];
+    buf[3 * S + li] = l2[1];
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) buf[(4 + 4 * mt + e) * 32 + lane] = o[mt][e];
+      for (int e = 0; e < 4; ++e) buf[(4 + 4 * mt + e) * S + li] = o[mt][e];
   };
-  auto merge_state = [&](const float* buf) {
+  auto merge_state_at = [&](const float* buf, int li, int S) {
     float a[2], bw[2];
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-      const float mb = buf[cc * 32 + lane];
+      const float mb = buf[cc * S + li];
       const float M = fmaxf(m2[cc], mb);
       if (M == -INFINITY) {
         a[cc] = 1.f;
@@ -525,14 +568,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         bw[cc] = exp2f(mb - M);
         m2[cc] = M;
       }
-      l2[cc] = a[cc] * l2[cc] + bw[cc] * buf[(2 + cc) * 32 + lane];
+      l2[cc] = a[cc] * l2[cc] + bw[cc] * buf[(2 + cc) * S + li];
     }
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        o[mt][e] = a[e & 1] * o[mt][e] + bw[e & 1] * buf[(4 + 4 * mt + e) * 32 + lane];
+        o[mt][e] = a[e & 1] * o[mt][e] + bw[e & 1] * buf[(4 + 4 * mt + e) * S + li];
   };
+  auto store_state = [&](float* buf) { store_state_at(buf, lane, 32); };
+  auto merge_state = [&](const float* buf) { merge_state_at(buf, lane, 32); };
 
   // ---- merging the partials of a segment this CTA completed (all threads).
   // Pass 1: the common maximum M per query head, all threads over all
@@ -545,8 +590,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
     const int64_t np = pfx[b + 1] - pfx[b];
     const int64_t s0 = (int64_t)p.Hkv * pfx[b] + (int64_t)h * np;
-    const int64_t c0 = cta_of(s0);
-    const int count = (int)(cta_of(s0 + np - 1) - c0 + 1);
+    const int64_t c0 = cta_of(s0, b, h);
+    const int count = (int)(cta_of(s0 + np - 1, b, h) - c0 + 1);
     const int64_t slot_base = c0 + seg;
     constexpr int kCols = G * D / 4;        // float4 columns of the output
     constexpr int kCPL = (kCols + 31) / 32;  // columns per lane
@@ -646,46 +691,137 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     if (tid == 0) p.tickets[seg] = 0;  // ready for the next call
   };
 
-  // A CTA learns it completed a split segment from the page-count ticket it
-  // added with a release atomic when it stored its partial.  Thread 0 checks
-  // the returned count only before the CTA's next barrier, so the atomic never
-  // stalls the stream; the merge then runs right after that barrier.
-  int pend_seg = -1, tk_old = 0, tk_add = 0, tk_np = 0;  // thread 0
-  auto resolve_ticket = [&]() {  // thread 0, before a CTA barrier
-    if (pend_seg >= 0) {
-      if (tk_old + tk_add == tk_np) {
-        __threadfence();  // acquire: the other contributors' partials
-        flag[1] = pend_seg;
+  // ---- merging the partials of a segment with one warp (no CTA barrier):
+  // the common maximum per query head first, then lane c takes float4 columns
+  // c, c+32, ... over all partials, in slot order.
+  auto merge_segment_warp = [&](int seg) {
+    const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+    const int64_t np = pfx[b + 1] - pfx[b];
+    const int64_t s0 = (int64_t)p.Hkv * pfx[b] + (int64_t)h * np;
+    const int64_t c0 = cta_of(s0, b, h);
+    const int count = (int)(cta_of(s0 + np - 1, b, h) - c0 + 1);
+    const int64_t slot_base = c0 + seg;
+    constexpr int kCols = G * D / 4;
+    constexpr int kCPL = (kCols + 31) / 32;
+    float mloc = -INFINITY;  // lane l: head l % G
+    for (int i = lane; i < count * G; i += 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot_base * G + i) * 2));
+      if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+    float4 acc[kCPL];
+    float lsum[kCPL], Mc[kCPL];
+#pragma unroll
+    for (int j = 0; j < kCPL; ++j) {
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      lsum[j] = 0.f;
+      const int col = lane + 32 * j;
+      Mc[j] = __shfl_sync(0xffffffffu, mloc, (col < kCols ? col : 0) / (D / 4));
+    }
+#pragma unroll 2
+    for (int kk = 0; kk < count; ++kk) {
+      const int64_t part = slot_base + kk;
+#pragma unroll
+      for (int j = 0; j < kCPL; ++j) {
+        const int col = lane + 32 * j;
+        if (col < kCols) {
+          const int head = col / (D / 4);
+          const float2 ml =
+              __ldcg(reinterpret_cast<const float2*>(p.part_ml + (part * G + head) * 2));
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + part * G * D) + col);
+          const float w = (ml.y > 0.f && Mc[j] > -INFINITY) ? exp2f(ml.x - Mc[j]) : 0.f;
+          lsum[j] += w * ml.y;
+          acc[j].x += w * v.x;
+          acc[j].y += w * v.y;
+          acc[j].z += w * v.z;
+          acc[j].w += w * v.w;
+        }
       }
-      pend_seg = -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kCPL; ++j) {
+      const int col = lane + 32 * j;
+      if (col < kCols) {
+        const int head = col / (D / 4);
+        const float inv = lsum[j] > 0.f ? 1.f / lsum[j] : 0.f;
+        const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
+        store_out_rt(p.out_dtype, p.out, ob + 0, acc[j].x * inv);
+        store_out_rt(p.out_dtype, p.out, ob + 1, acc[j].y * inv);
+        store_out_rt(p.out_dtype, p.out, ob + 2, acc[j].z * inv);
+        store_out_rt(p.out_dtype, p.out, ob + 3, acc[j].w * inv);
+      }
+    }
+    if (lane == 0) p.tickets[seg] = 0;  // ready for the next call
+  };
+
+  // A CTA learns it completed a split segment from the page-count ticket.
+  // The warp that stored a partial does not fence right away (under full
+  // memory load the fence waits microseconds for its stores to land): its
+  // lane 0 publishes it (fence, then an atomic add of its pages) at the CTA's
+  // next flush, when the stores are long done, and reads the atomic's result
+  // one flush later still (or at exit).
+  int pub_seg = -1, pub_add = 0;               // lane 0: partial stored, not yet published
+  int iss_seg = -1, iss_old = 0, iss_add = 0;  // lane 0: ticket added, result not yet read
+  int nflushes = 0;                            // the same in every warp
+  int k = 0;           // next ordinal this warp consumes
+  bool dead = false;   // a bounded wait gave up: skip compute and waits, keep the barriers
+  int k_dead = -1;     // first ordinal whose copy may still be in flight when dead
+  auto set_dead = [&](int from) {
+    if (!dead) {
+      dead = true;
+      k_dead = from;
+      if (lane == 0) report_error(p.err_word, PKV_ERR_TIMEOUT);
     }
   };
-  auto merge_if_flagged = [&]() {  // all threads, right after a CTA barrier
-    const int seg = flag[1];
-    if (seg >= 0) {
-      __threadfence();
-      merge_segment(seg);
-      merge_barrier();
-      if (tid == 0) flag[1] = -1;
+  auto seg_pages = [&](int seg) -> int {
+    const int b = seg / p.Hkv;
+    return pfx[b + 1] - pfx[b];
+  };
+  // lane 0: publish / resolve; m0, m1 get the segments this CTA completed
+  // (-1: none); only the final call waits for the atomic it issues
+  auto tickets_lane0 = [&](bool final_call, int& m0, int& m1) {
+    m0 = -1;
+    m1 = -1;
+    if (iss_seg >= 0) {
+      if (iss_old + iss_add == seg_pages(iss_seg)) m0 = iss_seg;
+      iss_seg = -1;
+    }
+    if (pub_seg >= 0) {
+      __threadfence();  // release: this warp's partial before its pages count
+      iss_old = atomicAdd(&p.tickets[pub_seg], pub_add);
+      iss_seg = pub_seg;
+      iss_add = pub_add;
+      pub_seg = -1;
+      if (final_call) {
+        if (iss_old + iss_add == seg_pages(iss_seg)) m1 = iss_seg;
+        iss_seg = -1;
+      }
+    }
+  };
+  auto tickets_step = [&](bool final_call) {  // every warp, before a CTA barrier
+    if (lane != 0) return;
+    int m0, m1;
+    tickets_lane0(final_call, m0, m1);
+    mflag[2 * warp] = m0;
+    mflag[2 * warp + 1] = m1;
+  };
+  auto merge_flagged = [&]() {  // all threads, right after a CTA barrier
+#pragma unroll 1
+    for (int i = 0; i < 2 * NW; ++i) {
+      const int seg = mflag[i];
+      if (seg >= 0) {
+        __threadfence();  // acquire: the other contributors' partials
+        merge_segment(seg);
+        merge_barrier();  // mbuf free again
+      }
     }
   };
 
-  // ---- end of this CTA's part of a segment: merge the 4 warps' states, then
-  // write the output (whole segment here) or this CTA's partial and ticket
-  auto flush = [&](int b, int h, bool split, int pages_mine) {
-    float* buf0 = mbuf;
-    float* buf1 = mbuf + C::kLaneState * 32;
-    if (tid == 0) resolve_ticket();
-    merge_barrier();
-    merge_if_flagged();  // uses mbuf, before the states go there
-    if (warp >= 2) store_state(warp == 2 ? buf0 : buf1);
-    merge_barrier();
-    if (warp < 2) merge_state(warp == 0 ? buf0 : buf1);
-    merge_barrier();
-    if (warp == 1) store_state(buf0);
-    merge_barrier();
-    if (warp != 0) return;
-    merge_state(buf0);
+  // ---- the merged state of a segment: write the output (whole segment in
+  // this share) or this CTA's partial (published at the next flush or exit)
+  auto finish = [&](int b, int h, bool split, int pages_mine) {
     const float vs = (CACHE == kCacheE4M3) ? p.v_scale[h] : 1.f;
     const int h0 = 2 * c4, h1 = 2 * c4 + 1;
     float lt0 = l2[0], lt1 = l2[1];
@@ -734,27 +870,87 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       }
     }
     __syncwarp();
-    if (lane == 0) {  // publish this partial's pages; the result is read later
-      const int seg = b * p.Hkv + h;
-      int old;
-      asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;"
-                   : "=r"(old) : "l"(&p.tickets[seg]), "r"(pages_mine) : "memory");
-      pend_seg = seg;
-      tk_old = old;
-      tk_add = pages_mine;
-      tk_np = pfx[b + 1] - pfx[b];
+    if (lane == 0) {
+      pub_seg = b * p.Hkv + h;
+      pub_add = pages_mine;
     }
   };
 
+  // ---- end of this CTA's part of a segment.  The warp that finishes (merges
+  // the four states and writes) rotates from flush to flush.
+  // Synchronous form (used when three warp states do not fit in mbuf): a
+  // tree of CTA barriers.
+  auto flush_sync = [&](int b, int h, bool split, int pages_mine) {
+    float* buf0 = mbuf;
+    float* buf1 = mbuf + C::kLaneState * 32;
+    const int wr = (warp - nflushes) & (NW - 1);  // this warp's role
+    ++nflushes;
+    tickets_step(false);
+    merge_barrier();
+    merge_flagged();  // uses mbuf, before the states go there
+    if (wr >= 2) store_state(wr == 2 ? buf0 : buf1);
+    merge_barrier();
+    if (wr < 2) merge_state(wr == 0 ? buf0 : buf1);
+    merge_barrier();
+    if (wr == 1) store_state(buf0);
+    merge_barrier();
+    if (wr != 0) return;
+    merge_state(buf0);
+    finish(b, h, split, pages_mine);
+  };
+  // Asynchronous form (G <= 4): the three other warps drop the lanes of their
+  // state that hold real heads into mbuf slots, arrive on the "full"
+  // mbarrier and go on with the next segment at once, so their copies keep
+  // streaming; the finisher waits on "full", merges, frees the slots through
+  // the "empty" mbarrier and writes.  A segment this warp's ticket completed
+  // is merged by this warp alone.
+  // Flush n uses full[n % 2] (its phase n / 2) and empty (its phase n).  No
+  // wait can see a barrier two phases away from the one it tests: the
+  // finisher of flush n was a writer at flush n - 1 and waited there for
+  // empty phase n - 2, which the finisher of flush n - 2 completed only
+  // after full[n % 2] completed its phase for flush n - 2; a writer of flush
+  // n waits for empty phase n - 1, and every earlier phase of empty was
+  // waited for by the warps whose arrivals complete phase n - 1.
+  constexpr int kU = G >= 4 ? G / 2 : 1;       // C-fragment columns pairs with real heads
+  constexpr int kCS = C::kLaneState * 8 * kU;  // floats per compact warp state
+  constexpr bool kAsyncFlush = G <= 4 && (NW - 1) * kCS <= 2 * C::kLaneState * 32;
+  auto flush_async = [&](int b, int h, bool split, int pages_mine) {
+    const int n = nflushes++;
+    const int fin = n & (NW - 1);
+    const uint32_t bar_full = smem_u32(fbar + (n & 1)), bar_empty = smem_u32(fbar + 2);
+    int m0 = -1, m1 = -1;
+    if (lane == 0) tickets_lane0(false, m0, m1);
+    m0 = __shfl_sync(0xffffffffu, m0, 0);
+    if (m0 >= 0) {
+      __threadfence();  // acquire: the other contributors' partials
+      merge_segment_warp(m0);
+    }
+    const int li = r8 * kU + c4;
+    if (warp != fin) {
+      if (n > 0 && !dead && !mbar_wait_bounded(bar_empty, (uint32_t)((n - 1) & 1), kWaitLimitNs))
+        set_dead(k);
+      if (c4 < kU) store_state_at(mbuf + ((warp - fin - 1) & (NW - 1)) * kCS, li, 8 * kU);
+      mbar_arrive(bar_full);
+      return;
+    }
+    if (!dead && !mbar_wait_bounded(bar_full, (uint32_t)((n >> 1) & 1), kWaitLimitNs)) set_dead(k);
+    if (c4 < kU) {
+#pragma unroll 1
+      for (int sl = 0; sl < NW - 1; ++sl) merge_state_at(mbuf + sl * kCS, li, 8 * kU);
+    }
+    mbar_arrive(bar_empty);
+    finish(b, h, split, pages_mine);
+  };
+  auto flush = [&](int b, int h, bool split, int pages_mine) {
+    if constexpr (kAsyncFlush) flush_async(b, h, split, pages_mine);
+    else flush_sync(b, h, split, pages_mine);
+  };
+
   // ---- main loop over the pieces of this CTA's share
-  bool dead = false;  // a bounded wait gave up: skip compute, keep the barriers
-  int k_dead = -1;
-  int k = 0;          // next ordinal to consume
   int ord_base = 0;   // first ordinal of the current piece (this warp)
   int cur_b = -1, cur_h = -1, pages_mine = 0;
   bool split = false;  // the current segment is shared with other CTAs
   bool have_q = false;
-  if (tid == 0) flag[1] = -1;
   for (int n = 0;; ++n) {
     const int2 R = (n == 0) ? r0 : piece(n);
     if (R.x >= R.y) break;  // no more work (later pieces are empty too)
@@ -791,11 +987,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         const int2 dsc = desc[k % kDescRing];
         const int slot = k % kS;
         if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + slot]),
-                                        (uint32_t)((k / kS) & 1), kWaitLimitNs)) {
-          dead = true;
-          k_dead = k;
-          if (lane == 0) report_error(p.err_word, PKV_ERR_TIMEOUT);
-        }
+                                        (uint32_t)((k / kS) & 1), kWaitLimitNs))
+          set_dead(k);
         if (!dead && dsc.x >= 0 && dsc.y > 0)
           compute_page(ring + (uint32_t)(slot * C::kStageBytes), dsc.y);
         __syncwarp();
@@ -812,12 +1005,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     ord_base += warp_count(R);
   }
   if (cur_b >= 0) flush(cur_b, cur_h, split, pages_mine);
-  if (tid == 0) resolve_ticket();
+  tickets_step(true);
   merge_barrier();
-  merge_if_flagged();
+  merge_flagged();
   if (dead) {
     // let the copies this warp still has in flight land (bounded) before exit
-    for (int q = k_dead + 1; q < issued; ++q)
+    for (int q = k_dead; q < issued; ++q)
       mbar_wait_bounded(smem_u32(&bars[warp * kS + (q % kS)]), (uint32_t)((q / kS) & 1),
                         kWaitLimitNs);
   }

@@ -20,16 +20,20 @@ enum CacheKind { kCacheF16 = 0, kCacheBF16 = 1, kCacheE4M3 = 2 };
 // the batch is small) and is walked in pieces of at most kRangeMax pages.
 constexpr int kRangeMin = 8;
 constexpr int kRangeMax = 64;
+// Cost of starting a (sequence, KV head) segment, in pages, when shares are
+// cut (a state merge, an output write and a pipeline refill).
+constexpr int kSegCost = 6;
 
 // Shared-memory plan of the decode kernel (host and device agree on it).
 constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
 constexpr int decode_stage_bytes(int d, CacheKind c) {
   return 2 * kPageSize * d * (c == kCacheE4M3 ? 1 : 2);
 }
-// alignment slack + descriptor rings + merge buffers + flags + mbarriers (8 max)
+// alignment slack + descriptor rings + merge buffers + merge flags +
+// mbarriers (8 stages max per warp, 4 slots for the flush hand-off)
 constexpr int decode_fixed_smem(int d) {
-  return 1024 + kDecodeWarps * 64 * 8 + 2 * decode_lane_state(d) * 32 * 4 + 16 +
-         kDecodeWarps * 8 * 8;
+  return 1024 + kDecodeWarps * 64 * 8 + 2 * decode_lane_state(d) * 32 * 4 +
+         2 * kDecodeWarps * 4 + kDecodeWarps * 8 * 8 + 32;
 }
 // Ring depth: as many K+V page slots per warp as fit two CTAs per SM (228 KB
 // per SM, 1 KB reserved per CTA) with room for the per-sequence arrays of a
@@ -87,7 +91,7 @@ struct AppendParams {
 inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
   return (size_t)decode_fixed_smem(d) +
          (size_t)kDecodeWarps * decode_stages(d, cache) * decode_stage_bytes(d, cache) +
-         (size_t)(2 * B + 1) * 4;
+         (size_t)(3 * B + 2) * 4;
 }
 
 // Returns a CUDA error (cudaSuccess when the kernel was enqueued) or
