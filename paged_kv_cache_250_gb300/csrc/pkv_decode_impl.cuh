@@ -579,181 +579,60 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   auto store_state = [&](float* buf) { store_state_at(buf, lane, 32); };
   auto merge_state = [&](const float* buf) { merge_state_at(buf, lane, 32); };
 
-  // ---- merging the partials of a segment this CTA completed (all threads).
-  // Pass 1: the common maximum M per query head, all threads over all
-  // partials.  Pass 2: warp w takes partials w, w+4, ...; lane c takes float4
-  // columns c, c+32, ...; weighted sums with independent loads; then the four
-  // warps' sums are added in shared memory and the output written.
-  auto merge_segment = [&](int seg) {
-    // the partials of CTAs cta_of(first unit) .. cta_of(last unit), stored
-    // under slots cta + seg
+  // ---- merging the partials of a completed segment.  Threads t, t+T, ...
+  // (T threads: one warp mid-kernel, the whole CTA at exit) take float4
+  // columns t, t+T, ...; each column finds its head's common maximum M over
+  // the partials, then adds them in slot order, so the result is bitwise the
+  // same whichever form runs.  No shared memory, no barrier.
+  auto merge_cols = [&](int seg, int t, int T) {
     const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
     const int64_t np = pfx[b + 1] - pfx[b];
     const int64_t s0 = (int64_t)p.Hkv * pfx[b] + (int64_t)h * np;
     const int64_t c0 = cta_of(s0, b, h);
     const int count = (int)(cta_of(s0 + np - 1, b, h) - c0 + 1);
-    const int64_t slot_base = c0 + seg;
-    constexpr int kCols = G * D / 4;        // float4 columns of the output
-    constexpr int kCPL = (kCols + 31) / 32;  // columns per lane
-    // shared buffers (inside the 2 * kLaneState * 32 floats of mbuf):
-    // Mh [NW][8] maxima, Lr [NW][8] sums, red [NW][kHalf] float4 warp sums
-    constexpr int kBudget = (2 * C::kLaneState * 32 - 2 * NW * 8) / (4 * NW);
-    constexpr int kHalf = kCols < (kBudget & ~31) ? kCols : (kBudget & ~31);
-    static_assert(kHalf >= (kCols < 32 ? kCols : 32), "merge buffer too small");
-    float* Mh = mbuf;
-    float* Lr = mbuf + NW * 8;
-    float4* red = reinterpret_cast<float4*>(mbuf + 2 * NW * 8);
-    // pass 1
-    float mloc = -INFINITY;
-    for (int i = tid; i < count * G; i += NW * 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot_base * G + i) * 2));
-      if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
-    }
-    for (int off = G; off < 32; off <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-    if (lane < G) Mh[warp * 8 + lane] = mloc;
-    merge_barrier();
-    // pass 2, kHalf columns per round (a head's columns never straddle two
-    // rounds: D / 4 divides kHalf)
-    constexpr int kCPR = (kHalf + 31) / 32;  // columns per lane per round
-    static_assert(kHalf % (D / 4) == 0 || kHalf == kCols, "head split across rounds");
+    const int64_t slot_base = c0 + seg;  // the partials of CTAs c0 .. c0 + count - 1
+    constexpr int kCols = G * D / 4;
 #pragma unroll 1
-    for (int r0 = 0; r0 < kCols; r0 += kHalf) {
-      float4 acc[kCPR];
-      float lsum[kCPR];
-      float Mc[kCPR];
-#pragma unroll
-      for (int j = 0; j < kCPR; ++j) {
-        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        lsum[j] = 0.f;
-        const int col = r0 + lane + 32 * j;
-        const int head = (col < kCols ? col : 0) / (D / 4);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, Mh[w * 8 + head]);
-        Mc[j] = M;
+    for (int col = t; col < kCols; col += T) {
+      const int head = col / (D / 4);
+      const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + slot_base * G + head;
+      const float4* vo = reinterpret_cast<const float4*>(p.part_o + slot_base * G * D) + col;
+      float M = -INFINITY;
+#pragma unroll 4
+      for (int kk = 0; kk < count; ++kk) {
+        const float2 v = __ldcg(ml + (int64_t)kk * G);
+        if (v.y > 0.f) M = fmaxf(M, v.x);
       }
-#pragma unroll 2
-      for (int kk = warp; kk < count; kk += NW) {
-        const int64_t part = slot_base + kk;
-#pragma unroll
-        for (int j = 0; j < kCPR; ++j) {
-          const int col = r0 + lane + 32 * j;
-          if (lane + 32 * j < kHalf && col < kCols) {
-            const int head = col / (D / 4);
-            const float2 ml =
-                __ldcg(reinterpret_cast<const float2*>(p.part_ml + (part * G + head) * 2));
-            const float4 v =
-                __ldcg(reinterpret_cast<const float4*>(p.part_o + part * G * D) + col);
-            const float w = (ml.y > 0.f && Mc[j] > -INFINITY) ? exp2f(ml.x - Mc[j]) : 0.f;
-            lsum[j] += w * ml.y;
-            acc[j].x += w * v.x;
-            acc[j].y += w * v.y;
-            acc[j].z += w * v.z;
-            acc[j].w += w * v.w;
-          }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lsum = 0.f;
+      if (M > -INFINITY) {
+#pragma unroll 4
+        for (int kk = 0; kk < count; ++kk) {
+          const float2 v = __ldcg(ml + (int64_t)kk * G);
+          const float4 x = __ldcg(vo + (int64_t)kk * (G * D / 4));
+          const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+          lsum += w * v.y;
+          acc.x += w * x.x;
+          acc.y += w * x.y;
+          acc.z += w * x.z;
+          acc.w += w * x.w;
         }
       }
-      // add the warps' sums; a head's l is the same in every lane holding one
-      // of its columns
-      if (r0 > 0) merge_barrier();  // the previous round's readers are done
-#pragma unroll
-      for (int j = 0; j < kCPR; ++j) {
-        const int c = lane + 32 * j;
-        const int col = r0 + c;
-        if (c < kHalf && col < kCols) {
-          red[warp * kHalf + c] = acc[j];
-          if (col % (D / 4) == 0) Lr[warp * 8 + col / (D / 4)] = lsum[j];
-        }
-      }
-      merge_barrier();
-      for (int c = tid; c < kHalf && r0 + c < kCols; c += NW * 32) {
-        const int col = r0 + c;
-        const int head = col / (D / 4);
-        float4 t = red[c];
-        float L = Lr[head];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) {
-          const float4 v = red[w * kHalf + c];
-          t.x += v.x;
-          t.y += v.y;
-          t.z += v.z;
-          t.w += v.w;
-          L += Lr[w * 8 + head];
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
-        store_out_rt(p.out_dtype, p.out, ob + 0, t.x * inv);
-        store_out_rt(p.out_dtype, p.out, ob + 1, t.y * inv);
-        store_out_rt(p.out_dtype, p.out, ob + 2, t.z * inv);
-        store_out_rt(p.out_dtype, p.out, ob + 3, t.w * inv);
-      }
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
+      store_out_rt(p.out_dtype, p.out, ob + 0, acc.x * inv);
+      store_out_rt(p.out_dtype, p.out, ob + 1, acc.y * inv);
+      store_out_rt(p.out_dtype, p.out, ob + 2, acc.z * inv);
+      store_out_rt(p.out_dtype, p.out, ob + 3, acc.w * inv);
     }
+  };
+  auto merge_segment = [&](int seg) {  // all threads
+    merge_cols(seg, tid, NW * 32);
     if (tid == 0) p.tickets[seg] = 0;  // ready for the next call
   };
-
-  // ---- merging the partials of a segment with one warp (no CTA barrier):
-  // the common maximum per query head first, then lane c takes float4 columns
-  // c, c+32, ... over all partials, in slot order.
-  auto merge_segment_warp = [&](int seg) {
-    const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
-    const int64_t np = pfx[b + 1] - pfx[b];
-    const int64_t s0 = (int64_t)p.Hkv * pfx[b] + (int64_t)h * np;
-    const int64_t c0 = cta_of(s0, b, h);
-    const int count = (int)(cta_of(s0 + np - 1, b, h) - c0 + 1);
-    const int64_t slot_base = c0 + seg;
-    constexpr int kCols = G * D / 4;
-    constexpr int kCPL = (kCols + 31) / 32;
-    float mloc = -INFINITY;  // lane l: head l % G
-    for (int i = lane; i < count * G; i += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot_base * G + i) * 2));
-      if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
-    }
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1)
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-    float4 acc[kCPL];
-    float lsum[kCPL], Mc[kCPL];
-#pragma unroll
-    for (int j = 0; j < kCPL; ++j) {
-      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      lsum[j] = 0.f;
-      const int col = lane + 32 * j;
-      Mc[j] = __shfl_sync(0xffffffffu, mloc, (col < kCols ? col : 0) / (D / 4));
-    }
-#pragma unroll 2
-    for (int kk = 0; kk < count; ++kk) {
-      const int64_t part = slot_base + kk;
-#pragma unroll
-      for (int j = 0; j < kCPL; ++j) {
-        const int col = lane + 32 * j;
-        if (col < kCols) {
-          const int head = col / (D / 4);
-          const float2 ml =
-              __ldcg(reinterpret_cast<const float2*>(p.part_ml + (part * G + head) * 2));
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + part * G * D) + col);
-          const float w = (ml.y > 0.f && Mc[j] > -INFINITY) ? exp2f(ml.x - Mc[j]) : 0.f;
-          lsum[j] += w * ml.y;
-          acc[j].x += w * v.x;
-          acc[j].y += w * v.y;
-          acc[j].z += w * v.z;
-          acc[j].w += w * v.w;
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kCPL; ++j) {
-      const int col = lane + 32 * j;
-      if (col < kCols) {
-        const int head = col / (D / 4);
-        const float inv = lsum[j] > 0.f ? 1.f / lsum[j] : 0.f;
-        const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
-        store_out_rt(p.out_dtype, p.out, ob + 0, acc[j].x * inv);
-        store_out_rt(p.out_dtype, p.out, ob + 1, acc[j].y * inv);
-        store_out_rt(p.out_dtype, p.out, ob + 2, acc[j].z * inv);
-        store_out_rt(p.out_dtype, p.out, ob + 3, acc[j].w * inv);
-      }
-    }
-    if (lane == 0) p.tickets[seg] = 0;  // ready for the next call
+  auto merge_segment_warp = [&](int seg) {  // one warp
+    merge_cols(seg, lane, 32);
+    if (lane == 0) p.tickets[seg] = 0;
   };
 
   // A CTA learns it completed a split segment from the page-count ticket.

@@ -192,9 +192,11 @@ def test_long_ragged_batch_is_repeatable_and_matches_the_oracle():
     w = wl.generate(cfg)
     run = GpuRun(w)
     out = run.step("f32").double().cpu().numpy()
-    out2 = run.decode("f32").double().cpu().numpy()
-    torch.cuda.synchronize()
-    assert np.array_equal(out, out2)
+    # which CTA merges a split segment, and when, depends on timing; the
+    # result must not
+    for _ in range(4):
+        again = run.decode("f32").double().cpu().numpy()
+        assert np.array_equal(out, again)
     assert_close(out, oracle_all(w), cfg, "f32", "long ragged batch")
 
 
