@@ -108,11 +108,14 @@ PKV_API pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache,
 /* Bytes of device workspace pkv_paged_decode_attention / pkv_decode_step
  * need for these sizes on the current device (it depends on the SM count).
  * Returns 0 on invalid arguments or without a device.  The workspace holds
- * one arrival counter per (sequence, KV head) and the split partials.  It
+ * the split partials and one arrival counter per (sequence, KV head).  It
  * must be zero-filled once before its first use (e.g. cudaMemsetAsync);
  * every call that completes leaves the counters at zero again, so it can be
- * reused without clearing.  After a call that reported PKV_ERR_TIMEOUT,
- * zero it again.  Calls that share a workspace must not overlap. */
+ * reused without clearing.  A workspace sized for a batch B serves every call
+ * with the same descriptor and a batch of at most B (any max_blocks_per_seq
+ * and hint); pass its full size.  After a call that reported
+ * PKV_ERR_TIMEOUT, zero it again.  Calls that share a workspace must not
+ * overlap. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t max_blocks_per_seq,
                                   int32_t max_context_len_hint);

@@ -80,14 +80,20 @@ pkv::CacheKind kind_of(pkv_dtype t) {
 }
 
 struct WsLayout {
-  size_t ticket_off, ml_off, o_off, total;
+  size_t ml_off, o_off, ticket_bytes, total;
   int ctas;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace: the per-segment page tickets (must start at zero; the kernel
-// returns them to zero), then ctas + segments partial slots (slot cta + seg).
+// Workspace: from the front, the split partials (one slot per CTA of the
+// largest grid plus one per segment, slot cta + seg); at the very end of the
+// caller's buffer, one page ticket per segment.  Only the tickets must be
+// zero when a call starts, and a completed call leaves them at zero.  The
+// partials' size grows with the batch and the tickets sit at the end, so a
+// workspace sized for batch B serves every call with the same descriptor and
+// a batch of at most B: a smaller call's tickets are the tail of a larger
+// call's, and no call's partials reach the tickets of any batch up to B.
 WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t hint,
                    int num_sms) {
   const int64_t g = d->num_q_heads / d->num_kv_heads;
@@ -101,23 +107,34 @@ WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t 
   const int64_t max_ctas = (int64_t)num_sms * pkv::kDecodeCtasPerSm;
   if (ctas > max_ctas) ctas = max_ctas;
   if (ctas < 1) ctas = 1;
-  const int64_t slots = ctas + segs;
+  const int64_t slots = max_ctas + segs;
   WsLayout w;
   w.ctas = (int)ctas;
-  w.ticket_off = 0;
-  w.ml_off = align256(w.ticket_off + (size_t)segs * sizeof(int32_t));
+  w.ml_off = 0;
   w.o_off = align256(w.ml_off + (size_t)slots * g * 2 * sizeof(float));
-  w.total = align256(w.o_off + (size_t)slots * g * d->head_dim * sizeof(float));
+  w.ticket_bytes = (size_t)segs * sizeof(int32_t);
+  w.total = align256(w.o_off + (size_t)slots * g * d->head_dim * sizeof(float) + w.ticket_bytes);
   return w;
+}
+
+// The tickets of a call: the last ticket_bytes of the caller's buffer.
+size_t ticket_offset(size_t workspace_bytes, const WsLayout& w) {
+  return (workspace_bytes & ~(size_t)3) - w.ticket_bytes;
 }
 
 }  // namespace
 
 namespace pkv {
-// Bytes at the start of a decode workspace that must be zero when a call
-// begins (the page tickets).
-size_t decode_workspace_zero_bytes(const pkv_cache_desc* d, int32_t batch) {
-  return align256((size_t)batch * d->num_kv_heads * sizeof(int32_t));
+cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,
+                                   const pkv_cache_desc* d, int32_t batch, int32_t mbs,
+                                   int32_t hint, cudaStream_t stream) {
+  int sms = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const WsLayout w = ws_layout(d, batch, mbs, hint, sms);
+  char* ws = static_cast<char*>(workspace);
+  return cudaMemsetAsync(ws + ticket_offset(workspace_bytes, w), 0, w.ticket_bytes, stream);
 }
 }  // namespace pkv
 
@@ -211,7 +228,7 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
   l.p.block_tables = block_tables;
   l.p.context_lens = context_lens;
   l.p.out = out;
-  l.p.tickets = reinterpret_cast<int32_t*>(ws + w.ticket_off);
+  l.p.tickets = reinterpret_cast<int32_t*>(ws + ticket_offset(workspace_bytes, w));
   l.p.part_ml = reinterpret_cast<float*>(ws + w.ml_off);
   l.p.part_o = reinterpret_cast<float*>(ws + w.o_off);
   l.p.k_scale = desc->k_scale;

@@ -319,11 +319,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   }
   const uint64_t pol = l2_policy_evict_first();
 
-  // the first two pieces and their descriptors need nothing the previous
-  // kernel writes (lengths and tables only)
-  const int2 r0 = piece(0), r1 = piece(1);
+  // the first piece and its descriptors need nothing the previous kernel
+  // writes (lengths and tables only); the second piece's lookups are issued
+  // when the first piece starts
+  const int2 r0 = piece(0);
   fill_desc(r0, 0);
-  fill_desc(r1, warp_count(r0));
 
   // From here on the kernel touches data the previous kernel on the stream may
   // write (cache pages, q, outputs, workspace): wait for it.
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   auto top_up = [&](int consumed) {  // keep kS loads in flight
     while (issued < consumed + kS && issued < filled_end) issue(issued++);
   };
-  filled_end = warp_count(r0) + warp_count(r1);
+  filled_end = warp_count(r0);
   top_up(0);
 
   // sequences with no tokens get a zero output row (spread over CTAs)
@@ -833,7 +833,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   for (int n = 0;; ++n) {
     const int2 R = (n == 0) ? r0 : piece(n);
     if (R.x >= R.y) break;  // no more work (later pieces are empty too)
-    if (n >= 1) fill_issue(piece(n + 1), ord_base + warp_count(R));
+    fill_issue(piece(n + 1), ord_base + warp_count(R));
     // the (b, h) segments inside piece R, in order
     int64_t x = R.x;
     while (x < R.y) {

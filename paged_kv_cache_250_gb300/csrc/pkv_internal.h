@@ -52,8 +52,8 @@ struct DecodeParams {
   const int32_t* block_tables; // [B][MBS]
   const int32_t* context_lens; // [B]
   void* out;                   // [B][Hq][d]
-  float* part_o;               // [ctas+B*Hkv][G][d] unnormalised partial outputs
-  float* part_ml;              // [ctas+B*Hkv][G][2] (reference max in log2 units, sum)
+  float* part_o;               // [max ctas+B*Hkv][G][d] unnormalised partial outputs
+  float* part_ml;              // [max ctas+B*Hkv][G][2] (reference max in log2 units, sum)
   int32_t* tickets;            // [B*Hkv]            pages stored per segment; zero between calls
   const float* k_scale;        // FP8 only
   const float* v_scale;        // FP8 only
@@ -99,9 +99,11 @@ inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
 cudaError_t launch_decode_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_e4m3(const DecodeLaunch& l);
-// Bytes at the start of a decode workspace that must be zero when a call
-// begins.
-size_t decode_workspace_zero_bytes(const pkv_cache_desc* d, int32_t batch);
+// Clears, on the stream, the parts of a decode workspace that must be zero
+// when a call begins (whatever an earlier, failed call left there).
+cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,
+                                   const pkv_cache_desc* d, int32_t batch, int32_t mbs,
+                                   int32_t hint, cudaStream_t stream);
 
 cudaError_t launch_append(const AppendParams& a, CacheKind cache, bool in_bf16,
                           cudaStream_t stream);

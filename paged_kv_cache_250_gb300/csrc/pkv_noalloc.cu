@@ -66,8 +66,9 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
   // the arrival counters must start at zero whatever an earlier call left
-  const size_t zero = pkv::decode_workspace_zero_bytes(desc, batch);
-  if (cudaMemsetAsync(scratch, 0, zero, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (pkv::decode_workspace_clear(scratch, (size_t)PKV_NOALLOC_SCRATCH_BYTES, desc, batch,
+                                  max_blocks_per_seq, max_context_len_hint,
+                                  reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKV_ERR_CUDA;
   return pkv_paged_decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens,
                                     batch, max_blocks_per_seq, max_context_len_hint, scale, out,

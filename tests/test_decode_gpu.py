@@ -200,6 +200,24 @@ def test_long_ragged_batch_is_repeatable_and_matches_the_oracle():
     assert_close(out, oracle_all(w), cfg, "f32", "long ragged batch")
 
 
+def test_one_workspace_across_workloads_of_different_sizes():
+    # a workspace sized for the larger batch serves calls with a smaller one
+    # in between: the tickets must stay zero and the partials apart
+    big = wl.small_config("big", 9, 32, 8, 128, "bf16", (200, 3000), seed=23)
+    small = wl.small_config("small", 3, 32, 8, 128, "bf16", (1, 40), seed=24)
+    wb, ws = wl.generate(big), wl.generate(small)
+    rb = GpuRun(wb)
+    rs = GpuRun(ws)
+    rs.workspace = rb.workspace  # shared; the big workload's size covers both
+    refb, refs = oracle_all(wb), oracle_all(ws)
+    rb.step("f32")
+    rs.step("f32")
+    for _ in range(3):
+        assert_close(rb.decode("f32").double().cpu().numpy(), refb, big, "f32", "big")
+        assert_close(rs.decode("f32").double().cpu().numpy(), refs, small, "f32", "small")
+    assert rb.err_code() == 0 and rs.err_code() == 0
+
+
 def test_prefix_sharing_tables():
     # sequence 1 shares sequence 0's first 3 blocks (48 tokens), then diverges
     cfg = wl.small_config("share", 2, 8, 2, 64, "f16", 1, seed=8, spare_blocks=0)
