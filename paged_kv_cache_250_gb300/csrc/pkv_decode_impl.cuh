@@ -64,6 +64,11 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr int kMergeBarrier = 1;                  // named barrier id (0 = __syncthreads)
 constexpr int kDescRing = 64;                     // page descriptors per warp
 
+template <int N>
+struct Int {  // a compile-time count passed to a generic lambda
+  static constexpr int value = N;
+};
+
 template <int D, int CACHE>
 struct DecodeCfg {
   static constexpr int kElem = CACHE == kCacheE4M3 ? 1 : 2;
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   constexpr int kS = C::kStages;
   constexpr int NW = kDecodeWarps;
   constexpr int kMT = C::kMTiles;
+  constexpr bool kPairs = kS >= 6;  // deep rings take pages two at a time
 
   if (!p.early_prologue) griddep_wait();
 
@@ -425,12 +431,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     if constexpr (CACHE == kCacheE4M3) c2 *= p.k_scale[h];
   };
 
-  auto compute_page = [&](uint32_t kt, int valid) {
-    const uint32_t vt = kt + C::kTileBytes;
-    // ---- S^T = K . Q^T
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+  // ---- S^T[16 tok][8] = K . Q^T for one page, on two accumulator chains
+  auto qk_page = [&](uint32_t kt, float (&s)[4]) {
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] = 0.f;
     if constexpr (CACHE != kCacheE4M3) {
-      float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: halves the MMA chain
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
         uint32_t a[4];
@@ -438,8 +444,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         if (ks & 1) mma_16816<kBF>(s2, a, qf[ks][0], qf[ks][1]);
         else mma_16816<kBF>(s, a, qf[ks][0], qf[ks][1]);
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] += s2[e];
     } else {
 #pragma unroll
       for (int gi = 0; gi < D / 32; ++gi) {
@@ -455,49 +459,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         a[1] = e4m3x2_to_f16x2(r[3]);
         a[2] = e4m3x2_to_f16x2(r[2] >> 16);
         a[3] = e4m3x2_to_f16x2(r[3] >> 16);
-        mma_16816<false>(s, a, qf[2 * gi + 1][0], qf[2 * gi + 1][1]);
+        mma_16816<false>(s2, a, qf[2 * gi + 1][0], qf[2 * gi + 1][1]);
       }
     }
-    // ---- online softmax (log2 domain); tokens past the context are masked
-    float x0 = s[0] * c2, x1 = s[1] * c2, x2 = s[2] * c2, x3 = s[3] * c2;
-    if (valid < kPageSize) {
-      if (r8 >= valid) x0 = x1 = -INFINITY;
-      if (r8 + 8 >= valid) x2 = x3 = -INFINITY;
-    }
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const bool grow = (mx0 > m2[0] + kRescaleThreshold) || (mx1 > m2[1] + kRescaleThreshold);
-    if (__any_sync(0xffffffffu, grow)) {
-      const float n0 = fmaxf(m2[0], mx0), n1 = fmaxf(m2[1], mx1);
-      const float a0 = exp2f(m2[0] - n0), a1 = exp2f(m2[1] - n1);
-      m2[0] = n0;
-      m2[1] = n1;
-      l2[0] *= a0;
-      l2[1] *= a1;
-#pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-        o[mt][0] *= a0;
-        o[mt][1] *= a1;
-        o[mt][2] *= a0;
-        o[mt][3] *= a1;
-      }
-    }
-    const float p0 = exp2f(x0 - m2[0]), p1 = exp2f(x1 - m2[1]);
-    const float p2 = exp2f(x2 - m2[0]), p3 = exp2f(x3 - m2[1]);
-    l2[0] += p0 + p2;
-    l2[1] += p1 + p3;
-    const uint32_t h01 = pack2<kBF>(p0, p1), h23 = pack2<kBF>(p2, p3);
-    const float2 f01 = unpack2<kBF>(h01), f23 = unpack2<kBF>(h23);
-    const uint32_t l01 = pack2<kBF>(p0 - f01.x, p1 - f01.y);
-    const uint32_t l23 = pack2<kBF>(p2 - f23.x, p3 - f23.y);
-    const uint32_t bh0 = movm_trans(h01), bh1 = movm_trans(h23);
-    const uint32_t bl0 = movm_trans(l01), bl1 = movm_trans(l23);
-    // ---- O^T += V^T . P^T ; V rows of masked tokens are zeroed (they may hold
-    // anything, and 0 * NaN would poison the sum)
+    for (int e = 0; e < 4; ++e) s[e] += s2[e];
+  };
+
+  // ---- O^T += V^T . P^T for one page; V rows of masked tokens are zeroed
+  // (they may hold anything, and 0 * NaN would poison the sum)
+  auto pv_page = [&](uint32_t vt, int valid, uint32_t bh0, uint32_t bh1, uint32_t bl0,
+                     uint32_t bl1) {
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (valid < kPageSize) {
       const int t0 = 2 * c4;
@@ -541,6 +513,67 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       }
     }
   };
+
+  // ---- NP (1 or 2) pages of one segment: their scores, one online-softmax
+  // update over all their tokens (log2 domain; tokens past the context are
+  // masked), then P.V.  Two pages give the warp two independent MMA chains
+  // and halve the reductions per token.
+  auto compute_pages = [&](auto npc, uint32_t ktA, int validA, uint32_t ktB, int validB) {
+    constexpr int NP = decltype(npc)::value;
+    float x[NP][4];
+    qk_page(ktA, x[0]);
+    if constexpr (NP == 2) qk_page(ktB, x[NP - 1]);
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int valid = i == 0 ? validA : validB;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[i][e] *= c2;
+      if (valid < kPageSize) {
+        if (r8 >= valid) x[i][0] = x[i][1] = -INFINITY;
+        if (r8 + 8 >= valid) x[i][2] = x[i][3] = -INFINITY;
+      }
+      mx0 = fmaxf(mx0, fmaxf(x[i][0], x[i][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[i][1], x[i][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const bool grow = (mx0 > m2[0] + kRescaleThreshold) || (mx1 > m2[1] + kRescaleThreshold);
+    if (__any_sync(0xffffffffu, grow)) {
+      const float n0 = fmaxf(m2[0], mx0), n1 = fmaxf(m2[1], mx1);
+      const float a0 = exp2f(m2[0] - n0), a1 = exp2f(m2[1] - n1);
+      m2[0] = n0;
+      m2[1] = n1;
+      l2[0] *= a0;
+      l2[1] *= a1;
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const float p0 = exp2f(x[i][0] - m2[0]), p1 = exp2f(x[i][1] - m2[1]);
+      const float p2 = exp2f(x[i][2] - m2[0]), p3 = exp2f(x[i][3] - m2[1]);
+      l2[0] += p0 + p2;
+      l2[1] += p1 + p3;
+      // P as hi + lo 16-bit parts, transposed into B fragments
+      const uint32_t h01 = pack2<kBF>(p0, p1), h23 = pack2<kBF>(p2, p3);
+      const float2 f01 = unpack2<kBF>(h01), f23 = unpack2<kBF>(h23);
+      const uint32_t l01 = pack2<kBF>(p0 - f01.x, p1 - f01.y);
+      const uint32_t l23 = pack2<kBF>(p2 - f23.x, p3 - f23.y);
+      const uint32_t kt = i == 0 ? ktA : ktB;
+      pv_page(kt + C::kTileBytes, i == 0 ? validA : validB, movm_trans(h01), movm_trans(h23),
+              movm_trans(l01), movm_trans(l23));
+    }
+  };
+  auto compute_page = [&](uint32_t kt, int valid) { compute_pages(Int<1>{}, kt, valid, 0u, 0); };
 
   // ---- merging warp states through shared memory: element i of the lane
   // state (m[2], l[2], o[MT][4]) at buf[i * S + li]
@@ -862,6 +895,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         if (!have_q) {
           load_q(b, h);
           have_q = true;
+        }
+        if constexpr (kPairs) {  // two pages of the segment at a time
+          if (j + 1 < j1) {
+            const int2 dA = desc[k % kDescRing], dB = desc[(k + 1) % kDescRing];
+            const int sA = k % kS, sB = (k + 1) % kS;
+            if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + sA]),
+                                            (uint32_t)((k / kS) & 1), kWaitLimitNs))
+              set_dead(k);
+            if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + sB]),
+                                            (uint32_t)(((k + 1) / kS) & 1), kWaitLimitNs))
+              set_dead(k + 1);
+            const bool okA = !dead && dA.x >= 0 && dA.y > 0;
+            const bool okB = !dead && dB.x >= 0 && dB.y > 0;
+            const uint32_t kA = ring + (uint32_t)(sA * C::kStageBytes);
+            const uint32_t kB = ring + (uint32_t)(sB * C::kStageBytes);
+            if (okA && okB) {
+              compute_pages(Int<2>{}, kA, dA.y, kB, dB.y);
+            } else {
+              if (okA) compute_page(kA, dA.y);
+              if (okB) compute_page(kB, dB.y);
+            }
+            __syncwarp();
+            if (fill_commit()) filled_end = f_ord + f_cnt;
+            if (!dead) top_up(k + 2);
+            ++j;
+            ++k;
+            continue;
+          }
         }
         const int2 dsc = desc[k % kDescRing];
         const int slot = k % kS;
