@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   constexpr int kS = C::kStages;
   constexpr int NW = kDecodeWarps;
   constexpr int kMT = C::kMTiles;
-  constexpr bool kPairs = kS >= 6;  // deep rings take pages two at a time
+  constexpr bool kPairs = kS >= 3;  // rings of 3+ pages take pages two at a time
 
   if (!p.early_prologue) griddep_wait();
 
