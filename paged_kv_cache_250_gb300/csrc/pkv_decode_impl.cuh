@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   constexpr int kS = C::kStages;
   constexpr int NW = kDecodeWarps;
   constexpr int kMT = C::kMTiles;
-  constexpr bool kPairs = kS >= 3;  // rings of 3+ pages take pages two at a time
+  // pages a warp takes per step: 2 on rings of 3+ pages (4 measured slower:
+  // longer P.V accumulation chains)
+  constexpr int kGroup = kS >= 3 ? 2 : 1;
 
   if (!p.early_prologue) griddep_wait();
 
@@ -514,19 +516,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
   };
 
-  // ---- NP (1 or 2) pages of one segment: their scores, one online-softmax
-  // update over all their tokens (log2 domain; tokens past the context are
-  // masked), then P.V.  Two pages give the warp two independent MMA chains
-  // and halve the reductions per token.
-  auto compute_pages = [&](auto npc, uint32_t ktA, int validA, uint32_t ktB, int validB) {
+  // ---- NP (1 or 2) pages of one segment: their scores, one online-
+  // softmax update over all their tokens (log2 domain; tokens past the
+  // context are masked), then P.V.  Several pages give the warp independent
+  // MMA chains and fewer reductions per token.
+  auto compute_pages = [&](auto npc, const uint32_t* kt, const int* valids) {
     constexpr int NP = decltype(npc)::value;
     float x[NP][4];
-    qk_page(ktA, x[0]);
-    if constexpr (NP == 2) qk_page(ktB, x[NP - 1]);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) qk_page(kt[i], x[i]);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const int valid = i == 0 ? validA : validB;
+      const int valid = valids[i];
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[i][e] *= c2;
       if (valid < kPageSize) {
@@ -568,12 +570,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const float2 f01 = unpack2<kBF>(h01), f23 = unpack2<kBF>(h23);
       const uint32_t l01 = pack2<kBF>(p0 - f01.x, p1 - f01.y);
       const uint32_t l23 = pack2<kBF>(p2 - f23.x, p3 - f23.y);
-      const uint32_t kt = i == 0 ? ktA : ktB;
-      pv_page(kt + C::kTileBytes, i == 0 ? validA : validB, movm_trans(h01), movm_trans(h23),
-              movm_trans(l01), movm_trans(l23));
+      pv_page(kt[i] + C::kTileBytes, valids[i], movm_trans(h01), movm_trans(h23), movm_trans(l01),
+              movm_trans(l23));
     }
   };
-  auto compute_page = [&](uint32_t kt, int valid) { compute_pages(Int<1>{}, kt, valid, 0u, 0); };
+  auto compute_page = [&](uint32_t kt, int valid) {
+    const uint32_t kt1[1] = {kt};
+    const int v1[1] = {valid};
+    compute_pages(Int<1>{}, kt1, v1);
+  };
 
   // ---- merging warp states through shared memory: element i of the lane
   // state (m[2], l[2], o[MT][4]) at buf[i * S + li]
@@ -896,31 +901,38 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
           load_q(b, h);
           have_q = true;
         }
-        if constexpr (kPairs) {  // two pages of the segment at a time
-          if (j + 1 < j1) {
-            const int2 dA = desc[k % kDescRing], dB = desc[(k + 1) % kDescRing];
-            const int sA = k % kS, sB = (k + 1) % kS;
-            if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + sA]),
-                                            (uint32_t)((k / kS) & 1), kWaitLimitNs))
-              set_dead(k);
-            if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + sB]),
-                                            (uint32_t)(((k + 1) / kS) & 1), kWaitLimitNs))
-              set_dead(k + 1);
-            const bool okA = !dead && dA.x >= 0 && dA.y > 0;
-            const bool okB = !dead && dB.x >= 0 && dB.y > 0;
-            const uint32_t kA = ring + (uint32_t)(sA * C::kStageBytes);
-            const uint32_t kB = ring + (uint32_t)(sB * C::kStageBytes);
-            if (okA && okB) {
-              compute_pages(Int<2>{}, kA, dA.y, kB, dB.y);
-            } else {
-              if (okA) compute_page(kA, dA.y);
-              if (okB) compute_page(kB, dB.y);
+        if constexpr (kGroup > 1) {  // several pages of the segment at a time
+          const int ng = (j1 - j >= kGroup) ? kGroup : 1;
+          if (ng > 1) {
+            uint32_t kt[kGroup];
+            int vv[kGroup];
+            bool all_ok = true;
+#pragma unroll
+            for (int i = 0; i < kGroup; ++i) {
+              if (i < ng) {
+                const int2 di = desc[(k + i) % kDescRing];
+                const int si = (k + i) % kS;
+                if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + si]),
+                                                (uint32_t)(((k + i) / kS) & 1), kWaitLimitNs))
+                  set_dead(k + i);
+                kt[i] = ring + (uint32_t)(si * C::kStageBytes);
+                vv[i] = (di.x >= 0) ? di.y : 0;
+                all_ok = all_ok && vv[i] > 0;
+              }
+            }
+            if (!dead) {
+              if (all_ok) {
+                compute_pages(Int<kGroup>{}, kt, vv);
+              } else {
+                for (int i = 0; i < ng; ++i)
+                  if (vv[i] > 0) compute_page(kt[i], vv[i]);
+              }
             }
             __syncwarp();
             if (fill_commit()) filled_end = f_ord + f_cnt;
-            if (!dead) top_up(k + 2);
-            ++j;
-            ++k;
+            if (!dead) top_up(k + ng);
+            j += ng - 1;
+            k += ng - 1;
             continue;
           }
         }

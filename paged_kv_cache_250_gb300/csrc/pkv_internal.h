@@ -16,9 +16,10 @@ constexpr int kDecodeCtasPerSm = 2;
 
 enum CacheKind { kCacheF16 = 0, kCacheBF16 = 1, kCacheE4M3 = 2 };
 
-// A CTA's share holds at least about kRangeMin pages (fewer CTAs run when
-// the batch is small) and is walked in pieces of at most kRangeMax pages.
-constexpr int kRangeMin = 8;
+// A CTA's share holds at least about kRangeMin cost units (fewer CTAs run
+// when the batch is small: a short context is not worth splitting) and is
+// walked in pieces of at most kRangeMax pages.
+constexpr int kRangeMin = 32;
 constexpr int kRangeMax = 64;
 // Cost of starting a (sequence, KV head) segment, in pages, when shares are
 // cut (a state merge, an output write and a pipeline refill).
