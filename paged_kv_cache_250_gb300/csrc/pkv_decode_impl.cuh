@@ -12,26 +12,31 @@
 // partial outputs are brought to a common maximum by the same factor).
 //
 // Schedule.  The (sequence b, KV head h, page) units are laid out b-major,
-// then h, then page, and cut into contiguous shares of equal cost, one per
-// CTA of a persistent grid (two CTAs per SM), so ragged lengths never leave
-// an SM idle; a page costs 1 and a segment start a few pages more.  A CTA walks its share in pieces of at most kRangeMax pages; page j
-// of a piece goes to warp j % 4, so the four warps move through the same
-// (b, h) "segment" together, each keeping its own online-softmax state.
-// When the share leaves a segment the four states are merged in shared
-// memory (the merge is order-independent).  A segment wholly inside one share
-// is normalised and written at once; a segment cut by share boundaries gets
-// one partial (m, l, o) per CTA, stored in slot cta + segment, and a
-// page-count ticket; the CTA whose pages complete the segment merges its
-// partials (the split combine), in slot order, at its next CTA barrier.
-// Nothing waits on another CTA, and every sum is taken in a fixed order, so
-// results are bitwise repeatable.
+// then h, then page, on a cost line where a page costs 1 and the start of a
+// (b, h) "segment" kSegCost more; the line is cut into contiguous shares of
+// equal cost (at least kRangeMin each), one per CTA of a persistent grid (two
+// CTAs per SM), so ragged lengths never leave an SM idle.  A CTA walks its
+// share in pieces of at most kRangeMax pages; page j of a piece goes to warp
+// j % 4, so the four warps move through the same segment together, each with
+// its own online-softmax state, taking two of their pages per step.
+//
+// Segment ends.  The four warp states are merged when the share leaves a
+// segment (the merge is order-independent): for groups of up to 4 query
+// heads three warps hand their state over through shared memory and an
+// mbarrier and keep streaming while a rotating fourth merges and writes; for
+// groups of 8 a tree of CTA barriers does it.  A segment wholly inside one
+// share is normalised and written at once; a segment cut by share boundaries
+// gets one partial (m, l, o) per CTA, in slot cta + segment, and a page-count
+// ticket; the CTA whose pages complete the segment merges the partials (the
+// split combine), in slot order.  Nothing waits on another CTA, and every
+// sum is taken in a fixed order, so results are bitwise repeatable.
 //
 // Data path per warp.  A ring of kStages shared-memory slots, each holding
 // one K page and one V page of one (block, KV head).  Lane 0 issues 2-D TMA
 // tile loads (128-byte swizzle, evict-first L2 policy) that complete on the
 // slot's mbarrier; the warp waits, computes, and refills the slot with its
-// page kStages ahead.  Block-table lookups for a range are done by the
-// warp's lanes in parallel into a descriptor ring in shared memory, one range
+// page kStages ahead.  Block-table lookups for a piece are done by the
+// warp's lanes in parallel into a descriptor ring in shared memory, one piece
 // ahead of their use.
 //
 // Math per page (16 tokens), all on warp-level tensor-core MMAs:
