@@ -127,6 +127,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def workload_config(cfg, ctx: torch.Tensor) -> dict:
+    """The workload keys both arms report in `config`."""
+    return {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
+            "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "page_size": wl.PAGE,
+            "cache_dtype": cfg.cache, "total_context_tokens": int(ctx.sum())}
+
+
 def algorithmic_bytes(cfg, ctx: torch.Tensor):
     """Bytes the step must move (read or write) at minimum.
 
@@ -319,9 +326,7 @@ def run_native(args, cfg, rank, world, device):
         "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[cfg.cache],
         "data": "synthetic (seeded N(0,1) q/k/v, uniform ragged context lengths, "
                 "permuted block tables)",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
-                   "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "page_size": wl.PAGE,
-                   "cache_dtype": cfg.cache, "total_context_tokens": int(st.w.ctx.sum()),
+        "config": {**workload_config(cfg, st.w.ctx),
                    "l2": f"rotating {R} cache-pool copies ({R * pool_bytes / 1e6:.0f} MB, "
                          f">= 4x L2); every step reads cold pages",
                    "timing": "K steps in one CUDA graph, CUDA events on the launch stream",
@@ -438,7 +443,9 @@ def run_reference(args, cfg):
             "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(1e3 * total_t / K, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, same generator as the native arm)",
-            "config": {"workload": cfg.name}, "cpu_baseline": cb,
+            "config": {**workload_config(cfg, w.ctx),
+                       "timing": "wall clock around each oracle pass on the host cores"},
+            "cpu_baseline": cb,
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
