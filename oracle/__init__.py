@@ -88,6 +88,8 @@ def _load():
         lib.pkvo_append_bytes.argtypes = [P, P, P, I32, I32, I32, I32, I32, I32]
         lib.pkvo_append_e4m3.restype = None
         lib.pkvo_append_e4m3.argtypes = [P, P, P, P, I32, I32, I32, I32, I32]
+        lib.pkvo_copy_blocks.restype = None
+        lib.pkvo_copy_blocks.argtypes = [P, P, P, I32, I32, I64]
         _lib = lib
         return lib
 
@@ -242,6 +244,22 @@ def append_e4m3(cache: np.ndarray, src, slot, head_scale) -> np.ndarray:
     slot = np.ascontiguousarray(np.asarray(slot, dtype=np.int64))
     _load().pkvo_append_e4m3(_ptr(out), _ptr(srcf), _ptr(slot), _ptr(hs),
                              slot.size, NB, P, Hkv, d)
+    return out
+
+
+def copy_blocks(cache: np.ndarray, src, dst) -> np.ndarray:
+    """Expected cache after copying block src[i] to block dst[i] (all heads,
+    in order); ids outside the pool are skipped.  Returns a new array.
+
+    cache: [NB][Hkv][P][d] of any element type.
+    """
+    out = np.ascontiguousarray(cache).copy()
+    src = np.ascontiguousarray(np.asarray(src, dtype=np.int32))
+    dst = np.ascontiguousarray(np.asarray(dst, dtype=np.int32))
+    assert src.shape == dst.shape
+    NB = out.shape[0]
+    block_bytes = out[0].nbytes if NB > 0 else 0
+    _load().pkvo_copy_blocks(_ptr(out), _ptr(src), _ptr(dst), src.size, NB, block_bytes)
     return out
 
 

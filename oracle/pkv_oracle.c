@@ -310,6 +310,25 @@ void pkvo_append_bytes(uint8_t* cache, const uint8_t* src, const int64_t* slot,
   }
 }
 
+/* ------------------------------------------------------------------ */
+/* Copy-on-write of whole blocks ([AP] "Paged attention: stop reserving */
+/* empty tables": sequences point at the same physical blocks for a    */
+/* shared beginning, copying only if one of them would change a block; */
+/* [KVFA] PagedAttention section: sharing a prefix hands the second     */
+/* sequence ceil(prefix / P) of the same blocks, so the last may be     */
+/* partly filled).  Block b of the cache is the [Hkv][P][d] run at      */
+/* b * block_bytes; dst[i] receives a copy of src[i]; pairs with either */
+/* id outside [0, NB) are skipped.                                      */
+/* ------------------------------------------------------------------ */
+void pkvo_copy_blocks(uint8_t* cache, const int32_t* src, const int32_t* dst, int32_t n,
+                      int32_t NB, int64_t block_bytes) {
+  for (int32_t i = 0; i < n; ++i) {
+    if (src[i] < 0 || src[i] >= NB || dst[i] < 0 || dst[i] >= NB) continue;
+    memmove(cache + (int64_t)dst[i] * block_bytes, cache + (int64_t)src[i] * block_bytes,
+            (size_t)block_bytes);
+  }
+}
+
 /* FP8 cache: the row is divided by the KV head's fp32 scale and encoded. */
 void pkvo_append_e4m3(uint8_t* cache, const float* src, const int64_t* slot,
                       const float* head_scale, int32_t T, int32_t NB, int32_t P,
