@@ -450,6 +450,54 @@ def run_reference(args, cfg):
                     "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- block copy
+def run_copy_blocks(args, device):
+    """pkv_copy_blocks alone: copy-on-write of whole blocks (8192 bf16 blocks of
+    8 KV heads x 16 tokens x 128, K and V: 1.07 GB read + 1.07 GB written per
+    step, far above L2), K steps in one CUDA graph, CUDA events around it."""
+    NB, Hkv, d, n = 16384, 8, 128, 8192
+    g = torch.Generator().manual_seed(7)
+    perm = torch.randperm(NB, generator=g).to(torch.int32)
+    src, dst = perm[:n].to(device), perm[n:2 * n].to(device)
+    kc = torch.randn(NB, Hkv, wl.PAGE, d, device=device).to(torch.bfloat16)
+    vc = torch.randn(NB, Hkv, wl.PAGE, d, device=device).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    desc = pkv.make_desc(NB, wl.PAGE, Hkv, Hkv, d, pkv.PKV_BF16, None, None, err)
+    stream = torch.cuda.Stream(device)
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        pkv.pkv_copy_blocks(desc, kc, vc, src, dst, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(K):
+            pkv.pkv_copy_blocks(desc, kc, vc, src, dst, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word set")
+    ms = e0.elapsed_time(e1) / K
+    nbytes = 2 * 2 * n * Hkv * wl.PAGE * d * 2  # K and V, read and written
+    value = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    return {"metric": "block copy (copy-on-write) achieved HBM GB/s", "value": round(value, 1),
+            "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) blocks)",
+            "config": {"workload": f"copy_blocks_{n}x_bf16_h{Hkv}_d{d}", "blocks": n,
+                       "block_bytes_per_cache": Hkv * wl.PAGE * d * 2,
+                       "timing": "K copies in one CUDA graph, CUDA events on the stream"},
+            "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
+                         "kernel": "copy_blocks_kernel", "peak_kind": peak_kind},
+            "gpu_launches": K}
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -459,6 +507,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode_step", choices=["decode_step", "copy_blocks"],
+                    help="decode_step (the default line) or copy_blocks alone")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -477,6 +527,10 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     pkv.load_library()
+    if args.op == "copy_blocks":
+        if rank == 0:
+            print(json.dumps(run_copy_blocks(args, device)), flush=True)
+        return
     res, st = run_native(args, cfg, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:

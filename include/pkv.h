@@ -204,6 +204,26 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
     int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
     pkv_dtype out_dtype, pkv_stream_t stream);
 
+/* Copy whole cache blocks, all KV heads of K and of V: block dst_blocks[i]
+ * receives block src_blocks[i], for i < n (copy-on-write for shared
+ * prefixes).  [AP] "Paged attention: stop reserving empty tables": sequences
+ * point at the same physical blocks for a shared beginning, copying only if
+ * one of them would change a block; [KVFA] PagedAttention section: sharing a
+ * prefix hands the second sequence ceil(prefix / P) of the same blocks, so
+ * the last may be partly filled and must be copied before either sequence
+ * appends into it.  The pages have no function of this name; it is the copy
+ * step of that scheme.
+ *   src_blocks, dst_blocks  device int32 [n].  A pair with an id outside
+ *                 [0, num_blocks) is skipped and reported as PKV_ERR_BOUNDS
+ *                 in err_word.  A block may be a destination at most once
+ *                 per call and must not also be a source in that call
+ *                 (the copies run concurrently).
+ * Asynchronous on `stream`; n == 0 launches nothing. */
+PKV_API pkv_status pkv_copy_blocks(const pkv_cache_desc* desc, void* k_cache,
+                                   void* v_cache, const int32_t* src_blocks,
+                                   const int32_t* dst_blocks, int32_t n,
+                                   pkv_stream_t stream);
+
 /* Cache bytes per token across all layers: 2 * layers * kv_heads * head_dim
  * * elem_bytes ([AP] "Opening the hood: how big is the notebook?"; [DF]
  * cache-size paragraph).  Host-only. */

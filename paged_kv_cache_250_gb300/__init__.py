@@ -9,6 +9,9 @@ memory and streams.  The functions carry the C names:
     pkv_paged_decode_attention    one (1,N) attention row per query head
     pkv_decode_step               both, validated together, the attention
                                   kernel overlapping the append's tail
+    pkv_copy_blocks               copy whole blocks (copy-on-write of a
+                                  shared prefix's last block)
+    pkv_paged_decode_attention_noalloc  decode without a caller workspace
     pkv_kv_bytes_per_token        cache bytes per token (host helper)
     pkv_status_string, pkv_version
 
@@ -31,7 +34,7 @@ __all__ = [
     "PkvError", "CacheDesc", "make_desc", "load_library", "library_path",
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
-    "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES",
+    "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES", "pkv_copy_blocks",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
     "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "EXPORTED_SYMBOLS",
@@ -44,7 +47,7 @@ PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
 EXPORTED_SYMBOLS = (
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
-    "pkv_paged_decode_attention_noalloc",
+    "pkv_paged_decode_attention_noalloc", "pkv_copy_blocks",
 )
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -107,6 +110,8 @@ def load_library():
         lib.pkv_paged_decode_attention_noalloc.restype = I32
         lib.pkv_paged_decode_attention_noalloc.argtypes = [D, P, P, P, P, P, I32, I32, I32,
                                                            ctypes.c_float, P, I32, I32, P]
+        lib.pkv_copy_blocks.restype = I32
+        lib.pkv_copy_blocks.argtypes = [D, P, P, P, P, I32, P]
         lib.pkv_kv_bytes_per_token.restype = U64
         lib.pkv_kv_bytes_per_token.argtypes = [I32, I32, I32, I32]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -177,6 +182,21 @@ def pkv_kv_append(desc: CacheDesc, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            _dev_ptr(k, "k"), _dev_ptr(v, "v"), int(k.shape[0]),
                            _DTYPE_CODE.get(k.dtype, -1), _stream_handle(stream, k.device))
     _check(st, "pkv_kv_append")
+
+
+def pkv_copy_blocks(desc: CacheDesc, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    src_blocks: torch.Tensor, dst_blocks: torch.Tensor, stream=None) -> None:
+    """Block dst_blocks[i] of both caches receives block src_blocks[i] (int32)."""
+    lib = load_library()
+    if src_blocks.dtype != torch.int32 or dst_blocks.dtype != torch.int32:
+        raise ValueError("block ids must be int32")
+    if src_blocks.numel() != dst_blocks.numel():
+        raise ValueError("src_blocks and dst_blocks must have the same length")
+    st = lib.pkv_copy_blocks(ctypes.byref(desc), _dev_ptr(k_cache, "k_cache"),
+                             _dev_ptr(v_cache, "v_cache"), _dev_ptr(src_blocks, "src_blocks"),
+                             _dev_ptr(dst_blocks, "dst_blocks"), int(src_blocks.numel()),
+                             _stream_handle(stream, k_cache.device))
+    _check(st, "pkv_copy_blocks")
 
 
 def pkv_decode_workspace_bytes(desc: CacheDesc, batch: int, max_blocks_per_seq: int,

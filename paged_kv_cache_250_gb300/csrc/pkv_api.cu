@@ -289,6 +289,30 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_copy_blocks(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                           const int32_t* src_blocks, const int32_t* dst_blocks, int32_t n,
+                           pkv_stream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (n < 0) return PKV_ERR_INVALID_ARG;
+  if (n == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_blocks, 4) ||
+      !aligned(dst_blocks, 4))
+    return PKV_ERR_INVALID_ARG;
+  pkv::CopyParams c;
+  c.k_cache = k_cache;
+  c.v_cache = v_cache;
+  c.src = src_blocks;
+  c.dst = dst_blocks;
+  c.err_word = desc->err_word;
+  c.block_bytes = (int64_t)desc->num_kv_heads * desc->page_size * desc->head_dim *
+                  (desc->cache_dtype == PKV_FP8_E4M3 ? 1 : 2);
+  c.NB = desc->num_blocks;
+  const cudaError_t e = pkv::launch_copy_blocks(c, n, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t max_blocks_per_seq, int32_t max_context_len_hint) {
   if (check_desc(desc) != PKV_OK || batch < 0 || max_blocks_per_seq <= 0) return 0;

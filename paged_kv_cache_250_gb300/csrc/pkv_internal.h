@@ -109,4 +109,16 @@ cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,
 cudaError_t launch_append(const AppendParams& a, CacheKind cache, bool in_bf16,
                           cudaStream_t stream);
 
+struct CopyParams {
+  void* k_cache;
+  void* v_cache;
+  const int32_t* src;
+  const int32_t* dst;
+  int32_t* err_word;
+  int64_t block_bytes;  // one block of one cache: Hkv * P * d * element bytes
+  int32_t NB;
+};
+
+cudaError_t launch_copy_blocks(const CopyParams& c, int32_t n, cudaStream_t stream);
+
 }  // namespace pkv

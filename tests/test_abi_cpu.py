@@ -78,6 +78,12 @@ def test_argument_errors_return_before_any_launch():
     bad.struct_size = 8
     st = lib.pkv_kv_append(ctypes.byref(bad), fake, fake, fake, fake, fake, 1, pkv.PKV_BF16, None)
     assert st == pkv.PKV_ERR_INVALID_ARG
+    # block copy: negative count, missing pointers; an empty copy is a no-op
+    assert lib.pkv_copy_blocks(ctypes.byref(good), fake, fake, fake, fake, -1, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(ctypes.byref(good), fake, None, fake, fake, 4, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(ctypes.byref(good), fake, fake, fake, fake, 0, None) == pkv.PKV_OK
     # unsupported page size / head dim / group; fp8 without scales
     for desc in (pkv.make_desc(64, 32, 2, 8, 128, pkv.PKV_BF16),
                  pkv.make_desc(64, 16, 2, 8, 80, pkv.PKV_BF16),
