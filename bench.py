@@ -59,6 +59,20 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (replicas run in lockstep between barriers)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(bytes_per_rank_step: int, ms_per_step: float, world: int) -> float:
+    """Throughput of all ranks together: each moves its own step's bytes."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -287,12 +301,7 @@ def run_native(args, cfg, rank, world, device):
         torch.cuda.synchronize(device)
         if world > 1:
             torch.distributed.barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), world, device)
 
     with torch.cuda.stream(stream):
         g_plain.replay()  # graph warm-up
@@ -315,7 +324,7 @@ def run_native(args, cfg, rank, world, device):
     append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
     decode_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
     ms_step = ms_total / K
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbps(step_bytes, ms_step, world)
     peak, peak_kind = measured_peak()
     achieved = attn_bytes / (decode_ms * 1e-3) / 1e9
     traffic = committed_traffic(cfg.name)
@@ -343,7 +352,7 @@ def run_native(args, cfg, rank, world, device):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "kernel": "decode_kernel "
                      "(pkv_paged_decode_attention, split combine fused)", "peak_kind": peak_kind},
-        "e2e": {"value": round(world * step_bytes / (ms_e2e / K * 1e-3) / 1e9, 1),
+        "e2e": {"value": round(whole_job_gbps(step_bytes, ms_e2e / K, world), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e / K, 5)},
         "gpu_launches": K * 2,
