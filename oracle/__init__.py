@@ -264,6 +264,20 @@ def copy_blocks(cache: np.ndarray, src, dst) -> np.ndarray:
 
 
 # ----------------------------------------------------------------- decode loop
+def multi_query_decode(q, K, V, scale: float) -> np.ndarray:
+    """Several new tokens of one sequence at once (verifying drafted tokens,
+    [KVFA] speculative-decoding section): q is [QL][d] for the last QL
+    positions of a sequence whose cached rows K, V are [n][d] (n >= QL, the
+    new tokens' rows included); query i sits at position n - QL + i and
+    attends to rows 0 .. n - QL + i, causal among the new tokens.  Each row
+    is the plain definition (attend_row)."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    n, QL = K.shape[0], q.shape[0]
+    assert n >= QL
+    return np.stack([attend_row(q[i], K[:n - QL + i + 1], V[:n - QL + i + 1], scale)
+                     for i in range(QL)])
+
+
 def causal_attention_last_row(X, Wq, Wk, Wv, scale: float) -> np.ndarray:
     """Recompute-everything step ([KVFA] opening section; [AP] "Arjun's first
     attempt"): project every token so far, form the full causal score matrix,
