@@ -159,6 +159,27 @@ PKV_API pkv_status pkv_paged_decode_attention(
     pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
     pkv_stream_t stream);
 
+/* Decode attention for q_len new tokens per sequence at once, causal among
+ * themselves (verifying drafted tokens: [KVFA] speculative-decoding section,
+ * where the target model scores the prefix and the drafted tokens in one
+ * forward pass).  Token j (0 <= j < q_len) of sequence b sits at position
+ * context_lens[b] - q_len + j and attends to positions 0 .. that position;
+ * the new tokens' K and V must already be in the cache (pkv_kv_append with
+ * batch * q_len rows), and context_lens counts them.  A token that sees no
+ * position (context_lens[b] < q_len) gets a zero row.
+ *   q, out        [batch][q_len][num_q_heads][head_dim].
+ *   q_len         1 .. 8 / (num_q_heads / num_kv_heads); larger returns
+ *                 PKV_ERR_UNSUPPORTED.  q_len 1 is pkv_paged_decode_attention.
+ * The workspace of pkv_decode_workspace_bytes serves any supported q_len.
+ * Other arguments and guarantees as for pkv_paged_decode_attention. */
+PKV_API pkv_status pkv_paged_decode_attention_multi(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t batch, int32_t q_len,
+    int32_t max_blocks_per_seq, int32_t max_context_len_hint, float scale,
+    void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
+
 /* One whole decode step: pkv_kv_append of one new token per sequence
  * (slot_mapping, k, v have `batch` rows) followed by
  * pkv_paged_decode_attention, validated together before anything is

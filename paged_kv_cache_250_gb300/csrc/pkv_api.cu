@@ -87,7 +87,8 @@ struct WsLayout {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace: from the front, the split partials (one slot per CTA of the
-// largest grid plus one per segment, slot cta + seg); at the very end of the
+// largest grid plus one per segment, slot cta + seg, each with room for the
+// 8 (query token, head) columns of a group); at the very end of the
 // caller's buffer, one page ticket per segment.  Only the tickets must be
 // zero when a call starts, and a completed call leaves them at zero.  The
 // partials' size grows with the batch and the tickets sit at the end, so a
@@ -96,7 +97,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // call's, and no call's partials reach the tickets of any batch up to B.
 WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t hint,
                    int num_sms) {
-  const int64_t g = d->num_q_heads / d->num_kv_heads;
+  // partial slots hold up to 8 (query token, head) columns, whatever the call
+  const int64_t g = 8;
   const int64_t cap = (int64_t)mbs * kPageSize;
   const int64_t len = (hint > 0 && hint < cap) ? hint : cap;
   const int64_t np_max = (len + kPageSize - 1) / kPageSize;
@@ -211,7 +213,7 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
                        const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
                        int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
                        pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                       pkv_stream_t stream, int early_prologue) {
+                       pkv_stream_t stream, int early_prologue, int32_t qlen = 1) {
   pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                                 max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
                                 out_dtype, workspace, workspace_bytes);
@@ -242,17 +244,33 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
   l.p.MBS = max_blocks_per_seq;
   l.p.out_dtype = out_dtype;
   l.p.early_prologue = early_prologue;
+  l.p.qlen = qlen;
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.group = desc->num_q_heads / desc->num_kv_heads;
+  // query-token capacity of the kernel: 1, or the smallest of 2, 4, 8 that
+  // holds qlen with group * capacity <= 8
+  l.qcap = 1;
+  if (qlen > 1) {
+    l.qcap = qlen <= 2 ? 2 : (qlen <= 4 ? 4 : 8);
+    if (l.group * l.qcap > 8) return PKV_ERR_UNSUPPORTED;
+  }
   l.cache = kind_of(desc->cache_dtype);
   l.q_bf16 = (q_dtype == PKV_BF16);
   l.ctas = w.ctas;
   l.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  switch (l.cache) {
-    case pkv::kCacheF16: e = pkv::launch_decode_f16(l); break;
-    case pkv::kCacheBF16: e = pkv::launch_decode_bf16(l); break;
-    default: e = pkv::launch_decode_e4m3(l); break;
+  if (l.qcap == 1) {
+    switch (l.cache) {
+      case pkv::kCacheF16: e = pkv::launch_decode_f16(l); break;
+      case pkv::kCacheBF16: e = pkv::launch_decode_bf16(l); break;
+      default: e = pkv::launch_decode_e4m3(l); break;
+    }
+  } else {
+    switch (l.cache) {
+      case pkv::kCacheF16: e = pkv::launch_decode_multi_f16(l); break;
+      case pkv::kCacheBF16: e = pkv::launch_decode_multi_bf16(l); break;
+      default: e = pkv::launch_decode_multi_e4m3(l); break;
+    }
   }
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -332,6 +350,21 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* desc, const void* q,
   return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                      max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
                      workspace, workspace_bytes, stream, /*early_prologue=*/0);
+}
+
+pkv_status pkv_paged_decode_attention_multi(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t batch, int32_t q_len,
+    int32_t max_blocks_per_seq, int32_t max_context_len_hint, float scale, void* out,
+    pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
+    pkv_stream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (q_len < 1) return PKV_ERR_INVALID_ARG;
+  if ((desc->num_q_heads / desc->num_kv_heads) * q_len > 8) return PKV_ERR_UNSUPPORTED;
+  return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                     max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                     workspace, workspace_bytes, stream, /*early_prologue=*/0, q_len);
 }
 
 pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, void* k_cache,

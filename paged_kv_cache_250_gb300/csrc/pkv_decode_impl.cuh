@@ -68,6 +68,9 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr int kMergeBarrier = 1;                  // named barrier id (0 = __syncthreads)
 constexpr int kDescRing = 64;                     // page descriptors per warp
+// A descriptor holds the tokens from the page's start to the context's end,
+// capped here (enough for the causal limits of up to 8 query tokens).
+constexpr int kRemCap = 2 * kPageSize;
 
 template <int N>
 struct Int {  // a compile-time count passed to a generic lambda
@@ -125,10 +128,15 @@ __device__ __forceinline__ void store_out_rt(pkv_dtype t, void* base, int64_t id
   else store_out<__half>(base, idx, v);
 }
 
-template <int D, int G, int CACHE, bool QBF16>
+// G query heads share a KV head; QC is the number of query tokens per
+// sequence the kernel is built for (p.qlen <= QC of them are real).  The
+// MMA's 8 columns hold the NC = QC * G (query token, head) pairs of a group.
+template <int D, int G, int QC, int CACHE, bool QBF16>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
+  constexpr int NC = G * QC;
+  static_assert(NC <= 8, "one MMA column per (query token, head)");
   using C = DecodeCfg<D, CACHE>;
   constexpr bool kBF = (CACHE == kCacheBF16);  // mma operand type (else fp16)
   constexpr int kS = C::kStages;
@@ -278,11 +286,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       int row = -1;
       if (blk >= 0 && blk < p.NB) row = (blk * p.Hkv + h) * kPageSize;
       else report_error(p.err_word, PKV_ERR_BOUNDS);
-      desc[(ord0 + j) % kDescRing] = make_int2(row, min(kPageSize, ctxs[b] - pg * kPageSize));
+      desc[(ord0 + j) % kDescRing] = make_int2(row, min(kRemCap, ctxs[b] - pg * kPageSize));
       if (j == 0 || pg == 0) {  // a segment may start here: warm its q rows in L2
-        const char* qp = reinterpret_cast<const char*>(p.q) + ((int64_t)b * p.Hq + h * G) * D * 2;
-        for (int off = 0; off < G * D * 2; off += 128)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + off));
+        for (int i = 0; i < p.qlen; ++i) {
+          const char* qp = reinterpret_cast<const char*>(p.q) +
+                           (((int64_t)b * p.qlen + i) * p.Hq + h * G) * D * 2;
+          for (int off = 0; off < G * D * 2; off += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + off));
+        }
       }
     }
     __syncwarp();
@@ -305,11 +316,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       f_h = (int)(rr / np);
       const int pg = (int)(rr - (int64_t)f_h * np);
       f_blk = p.block_tables[(int64_t)b * p.MBS + pg];
-      f_valid = min(kPageSize, ctxs[b] - pg * kPageSize);
+      f_valid = min(kRemCap, ctxs[b] - pg * kPageSize);
       if (lane == 0 || pg == 0) {  // a segment may start here: warm its q rows in L2
-        const char* qp = reinterpret_cast<const char*>(p.q) + ((int64_t)b * p.Hq + f_h * G) * D * 2;
-        for (int off = 0; off < G * D * 2; off += 128)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + off));
+        for (int i = 0; i < p.qlen; ++i) {
+          const char* qp = reinterpret_cast<const char*>(p.q) +
+                           (((int64_t)b * p.qlen + i) * p.Hq + f_h * G) * D * 2;
+          for (int off = 0; off < G * D * 2; off += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + off));
+        }
       }
     }
   };
@@ -372,8 +386,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   // sequences with no tokens get a zero output row (spread over CTAs)
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
     if (pfx[b + 1] != pfx[b]) continue;
-    const int64_t row0 = (int64_t)b * p.Hq * D;
-    for (int i = tid; i < p.Hq * D; i += blockDim.x) store_out_rt(p.out_dtype, p.out, row0 + i, 0.f);
+    const int64_t row0 = (int64_t)b * p.qlen * p.Hq * D;
+    for (int i = tid; i < p.qlen * p.Hq * D; i += blockDim.x)
+      store_out_rt(p.out_dtype, p.out, row0 + i, 0.f);
   }
 
   // ---- per-lane fragment coordinates
@@ -404,15 +419,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     l2[0] = l2[1] = 0.f;
   };
 
+  // row of q / out for MMA column c of segment (b, h): query token c / G,
+  // query head h * G + c % G; the column is real when c < G * p.qlen
+  auto col_row = [&](int b, int h, int c) -> int64_t {
+    return ((int64_t)b * p.qlen + c / G) * p.Hq + h * G + c % G;
+  };
+  auto col_real = [&](int c) -> bool { return c < NC && c < G * p.qlen; };
+
   auto load_q = [&](int b, int h) {
-    const int head = r8;  // B-fragment column n = lane / 4
+    const int col = r8;  // B-fragment column n = lane / 4
+    const bool real = col_real(col);
     const uint16_t* qrow =
-        reinterpret_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Hq + h * G + head) * D;
+        reinterpret_cast<const uint16_t*>(p.q) + (real ? col_row(b, h, col) : 0) * D;
     if constexpr (CACHE != kCacheE4M3) {
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
         uint32_t b0 = 0, b1 = 0;
-        if (head < G) {
+        if (real) {
           b0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4);
           b1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8);
         }
@@ -423,7 +446,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
         uint32_t b0 = 0, b1 = 0;
-        if (head < G) {
+        if (real) {
           const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c4);
           const float2 f01 = unpack2<QBF16>(raw4.x);
           const float2 f23 = unpack2<QBF16>(raw4.y);
@@ -533,12 +556,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const int valid = valids[i];
+      const int rem = valids[i];  // tokens from the page's start to the context's end
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[i][e] *= c2;
-      if (valid < kPageSize) {
-        if (r8 >= valid) x[i][0] = x[i][1] = -INFINITY;
-        if (r8 + 8 >= valid) x[i][2] = x[i][3] = -INFINITY;
+      if constexpr (QC == 1) {
+        if (rem < kPageSize) {
+          if (r8 >= rem) x[i][0] = x[i][1] = -INFINITY;
+          if (r8 + 8 >= rem) x[i][2] = x[i][3] = -INFINITY;
+        }
+      } else if (rem < kPageSize + QC - 1) {
+        // causal among the new tokens: query token j of the last qlen sees
+        // the page's first rem - (qlen - 1 - j) tokens
+        const int c0 = 2 * c4, c1 = 2 * c4 + 1;
+        const int l0 = col_real(c0) ? rem - (p.qlen - 1 - c0 / G) : rem;
+        const int l1 = col_real(c1) ? rem - (p.qlen - 1 - c1 / G) : rem;
+        if (r8 >= l0) x[i][0] = -INFINITY;
+        if (r8 >= l1) x[i][1] = -INFINITY;
+        if (r8 + 8 >= l0) x[i][2] = -INFINITY;
+        if (r8 + 8 >= l1) x[i][3] = -INFINITY;
       }
       mx0 = fmaxf(mx0, fmaxf(x[i][0], x[i][2]));
       mx1 = fmaxf(mx1, fmaxf(x[i][1], x[i][3]));
@@ -551,7 +586,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const bool grow = (mx0 > m2[0] + kRescaleThreshold) || (mx1 > m2[1] + kRescaleThreshold);
     if (__any_sync(0xffffffffu, grow)) {
       const float n0 = fmaxf(m2[0], mx0), n1 = fmaxf(m2[1], mx1);
-      const float a0 = exp2f(m2[0] - n0), a1 = exp2f(m2[1] - n1);
+      float a0 = exp2f(m2[0] - n0), a1 = exp2f(m2[1] - n1);
+      if constexpr (QC > 1) {  // a column that has seen nothing yet stays as it is
+        if (n0 == -INFINITY) a0 = 1.f;
+        if (n1 == -INFINITY) a1 = 1.f;
+      }
       m2[0] = n0;
       m2[1] = n1;
       l2[0] *= a0;
@@ -564,10 +603,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         o[mt][3] *= a1;
       }
     }
+    // a column every token so far was masked for keeps m = -inf: weigh its
+    // (all -inf) scores against 0, not -inf (only possible with QC > 1)
+    float mu0 = m2[0], mu1 = m2[1];
+    if constexpr (QC > 1) {
+      if (mu0 == -INFINITY) mu0 = 0.f;
+      if (mu1 == -INFINITY) mu1 = 0.f;
+    }
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const float p0 = exp2f(x[i][0] - m2[0]), p1 = exp2f(x[i][1] - m2[1]);
-      const float p2 = exp2f(x[i][2] - m2[0]), p3 = exp2f(x[i][3] - m2[1]);
+      const float p0 = exp2f(x[i][0] - mu0), p1 = exp2f(x[i][1] - mu1);
+      const float p2 = exp2f(x[i][2] - mu0), p3 = exp2f(x[i][3] - mu1);
       l2[0] += p0 + p2;
       l2[1] += p1 + p3;
       // P as hi + lo 16-bit parts, transposed into B fragments
@@ -575,8 +621,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const float2 f01 = unpack2<kBF>(h01), f23 = unpack2<kBF>(h23);
       const uint32_t l01 = pack2<kBF>(p0 - f01.x, p1 - f01.y);
       const uint32_t l23 = pack2<kBF>(p2 - f23.x, p3 - f23.y);
-      pv_page(kt[i] + C::kTileBytes, valids[i], movm_trans(h01), movm_trans(h23), movm_trans(l01),
-              movm_trans(l23));
+      pv_page(kt[i] + C::kTileBytes, valids[i] < kPageSize ? valids[i] : kPageSize, movm_trans(h01),
+              movm_trans(h23), movm_trans(l01), movm_trans(l23));
     }
   };
   auto compute_page = [&](uint32_t kt, int valid) {
@@ -634,16 +680,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const int64_t c0 = cta_of(s0, b, h);
     const int count = (int)(cta_of(s0 + np - 1, b, h) - c0 + 1);
     const int64_t slot_base = c0 + seg;  // the partials of CTAs c0 .. c0 + count - 1
-    constexpr int kCols = G * D / 4;
+    constexpr int kCols = NC * D / 4;
 #pragma unroll 1
     for (int col = t; col < kCols; col += T) {
-      const int head = col / (D / 4);
-      const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + slot_base * G + head;
-      const float4* vo = reinterpret_cast<const float4*>(p.part_o + slot_base * G * D) + col;
+      const int head = col / (D / 4);  // MMA column (query token, head)
+      if (!col_real(head)) continue;
+      const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + slot_base * NC + head;
+      const float4* vo = reinterpret_cast<const float4*>(p.part_o + slot_base * NC * D) + col;
       float M = -INFINITY;
 #pragma unroll 4
       for (int kk = 0; kk < count; ++kk) {
-        const float2 v = __ldcg(ml + (int64_t)kk * G);
+        const float2 v = __ldcg(ml + (int64_t)kk * NC);
         if (v.y > 0.f) M = fmaxf(M, v.x);
       }
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -651,8 +698,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       if (M > -INFINITY) {
 #pragma unroll 4
         for (int kk = 0; kk < count; ++kk) {
-          const float2 v = __ldcg(ml + (int64_t)kk * G);
-          const float4 x = __ldcg(vo + (int64_t)kk * (G * D / 4));
+          const float2 v = __ldcg(ml + (int64_t)kk * NC);
+          const float4 x = __ldcg(vo + (int64_t)kk * (NC * D / 4));
           const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
           lsum += w * v.y;
           acc.x += w * x.x;
@@ -662,7 +709,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const int64_t ob = ((int64_t)b * p.Hq + h * G + head) * D + (col % (D / 4)) * 4;
+      const int64_t ob = col_row(b, h, head) * D + (col % (D / 4)) * 4;
       store_out_rt(p.out_dtype, p.out, ob + 0, acc.x * inv);
       store_out_rt(p.out_dtype, p.out, ob + 1, acc.y * inv);
       store_out_rt(p.out_dtype, p.out, ob + 2, acc.z * inv);
@@ -755,17 +802,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     if (!split) {  // the whole segment was here: normalise and write
       const float i0 = lt0 > 0.f ? vs / lt0 : 0.f;
       const float i1 = lt1 > 0.f ? vs / lt1 : 0.f;
-      const int64_t ob = ((int64_t)b * p.Hq + h * G) * D;
+      const bool w0 = col_real(h0), w1 = col_real(h1);
+      const int64_t ob0 = (w0 ? col_row(b, h, h0) : 0) * D;
+      const int64_t ob1 = (w1 ? col_row(b, h, h1) : 0) * D;
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         const int dA = d_of(mt, 0), dB = d_of(mt, 1);
-        if (h0 < G) {
-          store_out_rt(p.out_dtype, p.out, ob + h0 * D + dA, o[mt][0] * i0);
-          store_out_rt(p.out_dtype, p.out, ob + h0 * D + dB, o[mt][2] * i0);
+        if (w0) {
+          store_out_rt(p.out_dtype, p.out, ob0 + dA, o[mt][0] * i0);
+          store_out_rt(p.out_dtype, p.out, ob0 + dB, o[mt][2] * i0);
         }
-        if (h1 < G) {
-          store_out_rt(p.out_dtype, p.out, ob + h1 * D + dA, o[mt][1] * i1);
-          store_out_rt(p.out_dtype, p.out, ob + h1 * D + dB, o[mt][3] * i1);
+        if (w1) {
+          store_out_rt(p.out_dtype, p.out, ob1 + dA, o[mt][1] * i1);
+          store_out_rt(p.out_dtype, p.out, ob1 + dB, o[mt][3] * i1);
         }
       }
       return;
@@ -773,20 +822,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     // partial slot cta + seg is unique: shares are contiguous and ordered, so
     // a later CTA never touches an earlier segment
     const int64_t part = (int64_t)blockIdx.x + b * p.Hkv + h;
-    float* po = p.part_o + part * G * D;
-    float* pml = p.part_ml + part * G * 2;
+    float* po = p.part_o + part * NC * D;
+    float* pml = p.part_ml + part * NC * 2;
     if (r8 == 0) {
-      if (h0 < G) { pml[2 * h0] = m2[0]; pml[2 * h0 + 1] = lt0; }
-      if (h1 < G) { pml[2 * h1] = m2[1]; pml[2 * h1 + 1] = lt1; }
+      if (h0 < NC) { pml[2 * h0] = m2[0]; pml[2 * h0 + 1] = lt0; }
+      if (h1 < NC) { pml[2 * h1] = m2[1]; pml[2 * h1 + 1] = lt1; }
     }
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) {
       const int dA = d_of(mt, 0), dB = d_of(mt, 1);
-      if (h0 < G) {
+      if (h0 < NC) {
         po[h0 * D + dA] = o[mt][0] * vs;
         po[h0 * D + dB] = o[mt][2] * vs;
       }
-      if (h1 < G) {
+      if (h1 < NC) {
         po[h1 * D + dA] = o[mt][1] * vs;
         po[h1 * D + dB] = o[mt][3] * vs;
       }
@@ -820,7 +869,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     merge_state(buf0);
     finish(b, h, split, pages_mine);
   };
-  // Asynchronous form (G <= 4): the three other warps drop the lanes of their
+  // Asynchronous form (NC <= 4): the three other warps drop the lanes of their
   // state that hold real heads into mbuf slots, arrive on the "full"
   // mbarrier and go on with the next segment at once, so their copies keep
   // streaming; the finisher waits on "full", merges, frees the slots through
@@ -833,9 +882,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   // after full[n % 2] completed its phase for flush n - 2; a writer of flush
   // n waits for empty phase n - 1, and every earlier phase of empty was
   // waited for by the warps whose arrivals complete phase n - 1.
-  constexpr int kU = G >= 4 ? G / 2 : 1;       // C-fragment columns pairs with real heads
+  constexpr int kU = NC >= 4 ? NC / 2 : 1;     // C-fragment column pairs with real columns
   constexpr int kCS = C::kLaneState * 8 * kU;  // floats per compact warp state
-  constexpr bool kAsyncFlush = G <= 4 && (NW - 1) * kCS <= 2 * C::kLaneState * 32;
+  constexpr bool kAsyncFlush = NC <= 4 && (NW - 1) * kCS <= 2 * C::kLaneState * 32;
   auto flush_async = [&](int b, int h, bool split, int pages_mine) {
     const int n = nflushes++;
     const int fin = n & (NW - 1);
@@ -974,10 +1023,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 }
 
 // ---------------------------------------------------------------------------
-// Host-side dispatch over head_dim and group for one cache kind.
-template <int D, int G, int CACHE, bool QBF16>
+// Host-side dispatch over head_dim, group and query tokens for one cache kind.
+template <int D, int G, int QC, int CACHE, bool QBF16>
 cudaError_t launch_split(const DecodeLaunch& l) {
-  auto kern = decode_kernel<D, G, CACHE, QBF16>;
+  auto kern = decode_kernel<D, G, QC, CACHE, QBF16>;
   const size_t smem = decode_smem_bytes(D, (CacheKind)CACHE, l.p.B);
   static size_t configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
@@ -999,16 +1048,35 @@ cudaError_t launch_split(const DecodeLaunch& l) {
   return cudaLaunchKernelEx(&cfg, kern, l.p, l.tmap_k, l.tmap_v);
 }
 
+// One query token per sequence.
 template <int CACHE, bool QBF16>
 cudaError_t dispatch_split(const DecodeLaunch& l) {
   const int d = l.p.d;
   const int g = l.group;
 #define PKV_CASE(DD, GG) \
-  if (d == DD && g == GG) return launch_split<DD, GG, CACHE, QBF16>(l);
+  if (d == DD && g == GG) return launch_split<DD, GG, 1, CACHE, QBF16>(l);
   if constexpr (CACHE != kCacheE4M3) {
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   }
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
+#undef PKV_CASE
+  return cudaErrorNotSupported;
+}
+
+// Several query tokens per sequence (l.qcap = 2, 4 or 8, with group * qcap <= 8).
+template <int CACHE, bool QBF16>
+cudaError_t dispatch_split_multi(const DecodeLaunch& l) {
+  const int d = l.p.d;
+  const int g = l.group;
+  const int qc = l.qcap;
+#define PKV_CASE(DD, GG, QQ) \
+  if (d == DD && g == GG && qc == QQ) return launch_split<DD, GG, QQ, CACHE, QBF16>(l);
+  if constexpr (CACHE != kCacheE4M3) {
+    PKV_CASE(64, 1, 2) PKV_CASE(64, 1, 4) PKV_CASE(64, 1, 8)
+    PKV_CASE(64, 2, 2) PKV_CASE(64, 2, 4) PKV_CASE(64, 4, 2)
+  }
+  PKV_CASE(128, 1, 2) PKV_CASE(128, 1, 4) PKV_CASE(128, 1, 8)
+  PKV_CASE(128, 2, 2) PKV_CASE(128, 2, 4) PKV_CASE(128, 4, 2)
 #undef PKV_CASE
   return cudaErrorNotSupported;
 }

@@ -61,6 +61,7 @@ struct DecodeParams {
   int32_t* err_word;
   int32_t B, Hq, Hkv, d, NB, MBS;
   pkv_dtype out_dtype;
+  int32_t qlen;                // query tokens per sequence (q, out are [B][qlen][Hq][d])
   int32_t early_prologue;      // 1: read lengths/tables before waiting on the previous kernel
   float scale_log2;            // softmax scale * log2(e)
 };
@@ -70,6 +71,7 @@ struct DecodeLaunch {
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
   int32_t group;               // Hq / Hkv
+  int32_t qcap;                // query tokens the kernel is built for (>= p.qlen)
   CacheKind cache;
   bool q_bf16;
   int32_t ctas;
@@ -100,6 +102,9 @@ inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
 cudaError_t launch_decode_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_e4m3(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_f16(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_bf16(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_e4m3(const DecodeLaunch& l);
 // Clears, on the stream, the parts of a decode workspace that must be zero
 // when a call begins (whatever an earlier, failed call left there).
 cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,
