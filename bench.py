@@ -507,6 +507,65 @@ def run_copy_blocks(args, device):
             "gpu_launches": K}
 
 
+# ---------------------------------------------------------------- multi-query
+def run_multi_query(args, cfg, device):
+    """pkv_paged_decode_attention_multi alone on a workload's cache: q_len new
+    tokens per sequence (already in the cache) attend at once, causal among
+    themselves.  K calls in one CUDA graph over rotating pool copies (>= 4x
+    L2), CUDA events around it; bytes as for one decode plus the extra q and
+    output rows."""
+    qlen = args.qlen
+    if cfg.group * qlen > 8:
+        raise SystemExit(f"q_len {qlen} x group {cfg.group} exceeds the 8 MMA columns")
+    hint = {"llama3_8b_b32_ctx1-4096_bf16": 4096}.get(cfg.name, 0)
+    st = Step(cfg, device, 1, hint)
+    pool_bytes = st.kc[0].numel() * st.kc[0].element_size() * 2
+    R = max(1, min(8, -(-4 * L2_BYTES // pool_bytes)))
+    st = Step(cfg, device, R, hint)
+    g = torch.Generator().manual_seed(cfg.seed + 77)
+    q = torch.randn(cfg.batch, qlen, cfg.q_heads, cfg.head_dim, generator=g).to(cfg.qdt).to(device)
+    out = torch.empty(cfg.batch, qlen, cfg.q_heads, cfg.head_dim, dtype=st.out.dtype, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def call(r):
+        pkv.pkv_paged_decode_attention_multi(st.desc, q, st.kc[r], st.vc[r], st.tables, st.ctx,
+                                             cfg.softmax_scale, out, st.ws, hint, stream=stream)
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        call(i % R)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(K):
+            call(i % R)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    if int(st.err.item()) != 0:
+        raise RuntimeError("device error word set")
+    ms = e0.elapsed_time(e1) / K
+    attn, _ = algorithmic_bytes(cfg, st.w.ctx)
+    attn += (qlen - 1) * cfg.batch * cfg.q_heads * cfg.head_dim * 4  # more q and out rows
+    value = attn / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    return {"metric": "multi-query decode-attention achieved HBM GB/s", "value": round(value, 1),
+            "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[cfg.cache],
+            "data": "synthetic (seeded N(0,1) q/k/v, the workload's lengths and tables)",
+            "config": {**workload_config(cfg, st.w.ctx), "q_len": qlen,
+                       "tokens_per_s_per_layer": round(cfg.batch * qlen / (ms * 1e-3), 1),
+                       "timing": "K calls in one CUDA graph, CUDA events on the stream"},
+            "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
+                         "kernel": f"decode_kernel (q_len {qlen})", "peak_kind": peak_kind},
+            "gpu_launches": K}
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -516,8 +575,10 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="decode_step", choices=["decode_step", "copy_blocks"],
-                    help="decode_step (the default line) or copy_blocks alone")
+    ap.add_argument("--op", default="decode_step",
+                    choices=["decode_step", "copy_blocks", "multi_query"],
+                    help="decode_step (the default line), copy_blocks or multi_query alone")
+    ap.add_argument("--qlen", type=int, default=2, help="query tokens per sequence (multi_query)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -539,6 +600,10 @@ def main():
     if args.op == "copy_blocks":
         if rank == 0:
             print(json.dumps(run_copy_blocks(args, device)), flush=True)
+        return
+    if args.op == "multi_query":
+        if rank == 0:
+            print(json.dumps(run_multi_query(args, cfg, device)), flush=True)
         return
     res, st = run_native(args, cfg, rank, world, device)
     if rank == 0:
