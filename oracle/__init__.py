@@ -278,6 +278,26 @@ def multi_query_decode(q, K, V, scale: float) -> np.ndarray:
                      for i in range(QL)])
 
 
+def window_decode(q, K, V, scale: float, window: int, sinks: int) -> np.ndarray:
+    """Multi-query decode under a sliding window with attention sinks ([AP]
+    "Sparse attention: stop looking at everything": each token sees only the
+    previous w tokens, and a few global tokens at the start of the text are
+    seen by everything; [KVFA] eviction paragraph: a sliding window drops the
+    oldest tokens, attention sinks always keep the first few).  Reading:
+    query j at position p = n - QL + j sees rows t <= p with t >= p - window + 1
+    (itself included) or t < sinks; window 0 means no window.  Each row is
+    attend_row over exactly those rows, in order."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    n, QL = K.shape[0], q.shape[0]
+    assert n >= QL and window >= 0 and sinks >= 0
+    out = []
+    for j in range(QL):
+        p = n - QL + j
+        rows = [t for t in range(p + 1) if window == 0 or t >= p - window + 1 or t < sinks]
+        out.append(attend_row(q[j], K[rows], V[rows], scale))
+    return np.stack(out)
+
+
 def causal_attention_last_row(X, Wq, Wk, Wv, scale: float) -> np.ndarray:
     """Recompute-everything step ([KVFA] opening section; [AP] "Arjun's first
     attempt"): project every token so far, form the full causal score matrix,

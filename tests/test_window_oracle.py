@@ -1,0 +1,43 @@
+"""Pins for the oracle's sliding-window decode with attention sinks ([AP]
+"Sparse attention: stop looking at everything"; [KVFA] eviction paragraph),
+against numpy brute force and the special cases that reduce to plainer
+results."""
+import numpy as np
+
+import oracle
+
+
+def _brute(Q, K, V, scale, window, sinks):
+    n, QL = K.shape[0], Q.shape[0]
+    S = (Q @ K.T) * scale
+    t = np.arange(n)[None, :]
+    p = np.arange(n - QL, n)[:, None]
+    vis = (t <= p) & ((window == 0) | (t >= p - window + 1) | (t < sinks))
+    S = np.where(vis, S, -np.inf)
+    S = S - S.max(axis=1, keepdims=True)
+    E = np.exp(S)
+    return (E / E.sum(axis=1, keepdims=True)) @ V
+
+
+def test_equals_brute_force_masks():
+    rng = np.random.default_rng(21)
+    for n, QL, w, s in [(50, 1, 16, 0), (50, 3, 16, 4), (100, 2, 33, 7), (40, 4, 64, 2),
+                        (70, 1, 5, 5), (33, 8, 10, 0)]:
+        Q, K, V = (rng.standard_normal((QL, 16)), rng.standard_normal((n, 16)),
+                   rng.standard_normal((n, 16)))
+        got = oracle.window_decode(Q, K, V, 0.25, w, s)
+        assert np.allclose(got, _brute(Q, K, V, 0.25, w, s), rtol=0, atol=1e-12)
+
+
+def test_special_cases():
+    rng = np.random.default_rng(22)
+    n, d = 30, 8
+    Q, K, V = rng.standard_normal((3, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    full = oracle.multi_query_decode(Q, K, V, 0.3)
+    # no window, a window covering everything, or sinks covering everything: full attention
+    assert np.array_equal(oracle.window_decode(Q, K, V, 0.3, 0, 0), full)
+    assert np.array_equal(oracle.window_decode(Q, K, V, 0.3, n, 0), full)
+    assert np.array_equal(oracle.window_decode(Q, K, V, 0.3, 1, n), full)
+    # a window of one and no sinks: each query sees only itself
+    one = oracle.window_decode(Q, K, V, 0.3, 1, 0)
+    assert np.array_equal(one, V[n - 3:])
