@@ -508,12 +508,26 @@ def run_copy_blocks(args, device):
 
 
 # ---------------------------------------------------------------- multi-query
-def run_multi_query(args, cfg, device):
-    """pkv_paged_decode_attention_multi alone on a workload's cache: q_len new
-    tokens per sequence (already in the cache) attend at once, causal among
-    themselves.  K calls in one CUDA graph over rotating pool copies (>= 4x
-    L2), CUDA events around it; bytes as for one decode plus the extra q and
-    output rows."""
+def visible_tokens(ctx: torch.Tensor, qlen: int, window: int, sinks: int) -> int:
+    """Cached positions at least one of a sequence's qlen new tokens sees
+    under a sliding window with sinks (window 0: all of them)."""
+    total = 0
+    for n in ctx.tolist():
+        if window <= 0:
+            total += n
+            continue
+        lo = max(0, n - qlen - window + 1)  # first position token 0's window reaches
+        total += (n - lo) + min(sinks, lo)
+    return total
+
+
+def run_multi_query(args, cfg, device, windowed: bool = False):
+    """pkv_paged_decode_attention_multi (or, windowed, _window) alone on a
+    workload's cache: q_len new tokens per sequence (already in the cache)
+    attend at once, causal among themselves.  K calls in one CUDA graph over
+    rotating pool copies (>= 4x L2), CUDA events around it; bytes as for one
+    decode plus the extra q and output rows, counting under a window only the
+    positions some token sees."""
     qlen = args.qlen
     if cfg.group * qlen > 8:
         raise SystemExit(f"q_len {qlen} x group {cfg.group} exceeds the 8 MMA columns")
@@ -528,8 +542,15 @@ def run_multi_query(args, cfg, device):
     stream = torch.cuda.Stream(device)
 
     def call(r):
-        pkv.pkv_paged_decode_attention_multi(st.desc, q, st.kc[r], st.vc[r], st.tables, st.ctx,
-                                             cfg.softmax_scale, out, st.ws, hint, stream=stream)
+        if windowed:
+            pkv.pkv_paged_decode_attention_window(st.desc, q, st.kc[r], st.vc[r], st.tables,
+                                                  st.ctx, args.window, args.sinks,
+                                                  cfg.softmax_scale, out, st.ws, hint,
+                                                  stream=stream)
+        else:
+            pkv.pkv_paged_decode_attention_multi(st.desc, q, st.kc[r], st.vc[r], st.tables,
+                                                 st.ctx, cfg.softmax_scale, out, st.ws, hint,
+                                                 stream=stream)
     K, W = args.steps, args.warmup
     for i in range(W):
         call(i % R)
@@ -550,19 +571,27 @@ def run_multi_query(args, cfg, device):
     ms = e0.elapsed_time(e1) / K
     attn, _ = algorithmic_bytes(cfg, st.w.ctx)
     attn += (qlen - 1) * cfg.batch * cfg.q_heads * cfg.head_dim * 4  # more q and out rows
+    extra = {"q_len": qlen}
+    if windowed:
+        kv_tok = cfg.kv_heads * cfg.head_dim * 2 * cfg.cache_elem_bytes
+        seen = visible_tokens(st.w.ctx, qlen, args.window, args.sinks)
+        attn -= (int(st.w.ctx.sum()) - seen) * kv_tok
+        extra.update(window=args.window, sinks=args.sinks, visible_tokens=seen)
     value = attn / (ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    return {"metric": "multi-query decode-attention achieved HBM GB/s", "value": round(value, 1),
+    what = "windowed" if windowed else "multi-query"
+    return {"metric": f"{what} decode-attention achieved HBM GB/s", "value": round(value, 1),
             "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[cfg.cache],
             "data": "synthetic (seeded N(0,1) q/k/v, the workload's lengths and tables)",
-            "config": {**workload_config(cfg, st.w.ctx), "q_len": qlen,
+            "config": {**workload_config(cfg, st.w.ctx), **extra,
                        "tokens_per_s_per_layer": round(cfg.batch * qlen / (ms * 1e-3), 1),
                        "timing": "K calls in one CUDA graph, CUDA events on the stream"},
             "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
-                         "kernel": f"decode_kernel (q_len {qlen})", "peak_kind": peak_kind},
+                         "kernel": f"decode_kernel (q_len {qlen}{', window' if windowed else ''})",
+                         "peak_kind": peak_kind},
             "gpu_launches": K}
 
 
@@ -576,9 +605,13 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="decode_step",
-                    choices=["decode_step", "copy_blocks", "multi_query"],
-                    help="decode_step (the default line), copy_blocks or multi_query alone")
-    ap.add_argument("--qlen", type=int, default=2, help="query tokens per sequence (multi_query)")
+                    choices=["decode_step", "copy_blocks", "multi_query", "window"],
+                    help="decode_step (the default line), copy_blocks, multi_query or window "
+                         "alone")
+    ap.add_argument("--qlen", type=int, default=2,
+                    help="query tokens per sequence (multi_query, window)")
+    ap.add_argument("--window", type=int, default=4096, help="window length (window)")
+    ap.add_argument("--sinks", type=int, default=4, help="sink positions (window)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -601,9 +634,9 @@ def main():
         if rank == 0:
             print(json.dumps(run_copy_blocks(args, device)), flush=True)
         return
-    if args.op == "multi_query":
+    if args.op in ("multi_query", "window"):
         if rank == 0:
-            print(json.dumps(run_multi_query(args, cfg, device)), flush=True)
+            print(json.dumps(run_multi_query(args, cfg, device, args.op == "window")), flush=True)
         return
     res, st = run_native(args, cfg, rank, world, device)
     if rank == 0:

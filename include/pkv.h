@@ -180,6 +180,30 @@ PKV_API pkv_status pkv_paged_decode_attention_multi(
     void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
     size_t workspace_bytes, pkv_stream_t stream);
 
+/* pkv_paged_decode_attention_multi under a sliding window with attention
+ * sinks ([AP] "Sparse attention: stop looking at everything": a token sees
+ * only the previous w tokens plus a few global tokens at the start; [KVFA]
+ * eviction paragraph: the window drops the oldest tokens, the first few are
+ * always kept).  Token j, at position t = context_lens[b] - q_len + j, attends
+ * to the positions u <= t with u >= t - window + 1 (itself included) or
+ * u < sinks.
+ *   window        0: no window (the call is pkv_paged_decode_attention_multi
+ *                 and sinks is ignored); > 0: the window length in tokens.
+ *   sinks         >= 0 leading positions every token keeps seeing.
+ * Pages that no token of the sequence sees (wholly between the sink pages
+ * and the first page of token 0's window) are neither loaded nor looked up:
+ * their block-table entries are never read and may be anything, so a caller
+ * may hand those blocks back to its pool.  Negative window or sinks, or
+ * q_len < 1, return PKV_ERR_INVALID_ARG.  Other arguments and guarantees as
+ * for pkv_paged_decode_attention_multi. */
+PKV_API pkv_status pkv_paged_decode_attention_window(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t batch, int32_t q_len, int32_t window,
+    int32_t sinks, int32_t max_blocks_per_seq, int32_t max_context_len_hint,
+    float scale, void* out, pkv_dtype q_dtype, pkv_dtype out_dtype,
+    void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
 /* One whole decode step: pkv_kv_append of one new token per sequence
  * (slot_mapping, k, v have `batch` rows) followed by
  * pkv_paged_decode_attention, validated together before anything is

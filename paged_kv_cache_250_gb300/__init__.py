@@ -8,6 +8,8 @@ memory and streams.  The functions carry the C names:
     pkv_decode_workspace_bytes    workspace size for a decode call
     pkv_paged_decode_attention    one (1,N) attention row per query head
     pkv_paged_decode_attention_multi  q_len new tokens per sequence, causal
+    pkv_paged_decode_attention_window  the same under a sliding window with
+                                  attention sinks
     pkv_decode_step               both, validated together, the attention
                                   kernel overlapping the append's tail
     pkv_copy_blocks               copy whole blocks (copy-on-write of a
@@ -36,7 +38,7 @@ __all__ = [
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES", "pkv_copy_blocks",
-    "pkv_paged_decode_attention_multi",
+    "pkv_paged_decode_attention_multi", "pkv_paged_decode_attention_window",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
     "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "EXPORTED_SYMBOLS",
@@ -50,6 +52,7 @@ EXPORTED_SYMBOLS = (
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "pkv_copy_blocks", "pkv_paged_decode_attention_multi",
+    "pkv_paged_decode_attention_window",
 )
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -115,6 +118,10 @@ def load_library():
         lib.pkv_paged_decode_attention_multi.restype = I32
         lib.pkv_paged_decode_attention_multi.argtypes = [D, P, P, P, P, P, I32, I32, I32, I32,
                                                          ctypes.c_float, P, I32, I32, P, SZ, P]
+        lib.pkv_paged_decode_attention_window.restype = I32
+        lib.pkv_paged_decode_attention_window.argtypes = [D, P, P, P, P, P, I32, I32, I32, I32,
+                                                          I32, I32, ctypes.c_float, P, I32, I32,
+                                                          P, SZ, P]
         lib.pkv_copy_blocks.restype = I32
         lib.pkv_copy_blocks.argtypes = [D, P, P, P, P, I32, P]
         lib.pkv_kv_bytes_per_token.restype = U64
@@ -254,6 +261,30 @@ def pkv_paged_decode_attention_multi(desc: CacheDesc, q: torch.Tensor, k_cache: 
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _stream_handle(stream, q.device))
     _check(st, "pkv_paged_decode_attention_multi")
+
+
+def pkv_paged_decode_attention_window(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
+                                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                      context_lens: torch.Tensor, window: int, sinks: int,
+                                      scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                                      max_context_len_hint: int = 0, stream=None) -> None:
+    """As pkv_paged_decode_attention_multi, token t seeing only positions
+    t - window + 1 .. t and the first `sinks` positions (window 0: no window)."""
+    lib = load_library()
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if q.dim() != 4 or out.shape != q.shape:
+        raise ValueError("q and out must be [B][q_len][Hq][d]")
+    B, mbs = int(block_tables.shape[0]), int(block_tables.shape[1])
+    st = lib.pkv_paged_decode_attention_window(
+        ctypes.byref(desc), _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(context_lens, "context_lens"), B, int(q.shape[1]), int(window), int(sinks),
+        mbs, int(max_context_len_hint), float(scale), _dev_ptr(out, "out"),
+        _DTYPE_CODE.get(q.dtype, -1), _DTYPE_CODE.get(out.dtype, -1),
+        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
+        _stream_handle(stream, q.device))
+    _check(st, "pkv_paged_decode_attention_window")
 
 
 def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,

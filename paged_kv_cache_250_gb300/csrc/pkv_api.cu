@@ -213,7 +213,8 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
                        const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
                        int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
                        pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                       pkv_stream_t stream, int early_prologue, int32_t qlen = 1) {
+                       pkv_stream_t stream, int early_prologue, int32_t qlen = 1,
+                       int32_t window = 0, int32_t sinks = 0) {
   pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                                 max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
                                 out_dtype, workspace, workspace_bytes);
@@ -245,6 +246,8 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
   l.p.out_dtype = out_dtype;
   l.p.early_prologue = early_prologue;
   l.p.qlen = qlen;
+  l.p.window = window;
+  l.p.sinks = window > 0 ? sinks : 0;
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.group = desc->num_q_heads / desc->num_kv_heads;
   // query-token capacity of the kernel: 1, or the smallest of 2, 4, 8 that
@@ -365,6 +368,22 @@ pkv_status pkv_paged_decode_attention_multi(
   return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                      max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
                      workspace, workspace_bytes, stream, /*early_prologue=*/0, q_len);
+}
+
+pkv_status pkv_paged_decode_attention_window(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t batch, int32_t q_len,
+    int32_t window, int32_t sinks, int32_t max_blocks_per_seq, int32_t max_context_len_hint,
+    float scale, void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
+    size_t workspace_bytes, pkv_stream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (q_len < 1 || window < 0 || sinks < 0) return PKV_ERR_INVALID_ARG;
+  if ((desc->num_q_heads / desc->num_kv_heads) * q_len > 8) return PKV_ERR_UNSUPPORTED;
+  return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                     max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                     workspace, workspace_bytes, stream, /*early_prologue=*/0, q_len, window,
+                     sinks);
 }
 
 pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, void* k_cache,

@@ -71,6 +71,8 @@ constexpr int kDescRing = 64;                     // page descriptors per warp
 // A descriptor holds the tokens from the page's start to the context's end,
 // capped here (enough for the causal limits of up to 8 query tokens).
 constexpr int kRemCap = 2 * kPageSize;
+constexpr int kRemMask = 63;       // descriptor y, bits 0-5: tokens to the context's end
+constexpr int kWinFlag = 1 << 17;  // descriptor: a sliding window masks rows of this page
 
 template <int N>
 struct Int {  // a compile-time count passed to a generic lambda
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   int32_t* pfx = mflag + 2 * NW;                                      // [B+1] pages
   int32_t* nzp = pfx + (p.B + 1);                                     // [B+1] non-empty seqs
   int32_t* ctxs = nzp + (p.B + 1);                                    // [B]
+  int32_t* gns = ctxs + p.B;  // [B] pages before a sliding window's gap (all pages if none)
+  int32_t* gsk = gns + p.B;   // [B] pages the gap skips
   const int64_t Gn = gridDim.x;
 
   // ---- prologue: pages per sequence, prefix sums of pages and of non-empty
@@ -185,8 +189,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     } else {
       np = (c + kPageSize - 1) / kPageSize;
     }
+    // with a sliding window the pages between the sink pages and the first
+    // page any query's window reaches are never read: a sequence's units are
+    // its visible pages only
+    int ns = np, sk = 0;
+    if (p.window > 0 && np > 0) {
+      const int lo = max(0, c - p.qlen - p.window + 1);  // first position of query 0's window
+      const int fw = lo / kPageSize;
+      const int nsp = (min(c, p.sinks) + kPageSize - 1) / kPageSize;
+      if (fw > nsp) {
+        ns = nsp;
+        sk = fw - nsp;
+      }
+    }
     ctxs[b] = c;
-    pfx[b + 1] = np;
+    gns[b] = ns;
+    gsk[b] = sk;
+    pfx[b + 1] = np - sk;
     nzp[b + 1] = np > 0 ? 1 : 0;
   }
   if (lane == 0) {
@@ -273,7 +292,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const int n = r.y - r.x - warp;
     return n > 0 ? (n + NW - 1) / NW : 0;
   };
-  auto fill_desc = [&](int2 r, int ord0) {  // {tma row or -1, valid tokens}
+  // A descriptor's y: tokens from the page's start to the context's end
+  // (capped at kRemCap), then, for a page a sliding window cuts, the rows
+  // before query 0's window start and the sink rows, and a flag.
+  auto page_info = [&](int b, int pg) -> int {
+    const int pos = pg * kPageSize;
+    int y = min(kRemCap, ctxs[b] - pos);
+    if (p.window > 0) {
+      const int wr = ctxs[b] - p.qlen - p.window + 1 - pos;  // query 0: rows >= wr visible
+      const int sr = p.sinks - pos;                          // rows < sr always visible
+      if (wr + p.qlen - 1 > 0 && sr < kPageSize) {
+        const int wrc = wr < -8 ? -8 : (wr > 24 ? 24 : wr);
+        const int src = sr < 0 ? 0 : sr;
+        y |= (src << 6) | ((wrc + 8) << 11) | kWinFlag;
+      }
+    }
+    return y;
+  };
+  auto fill_desc = [&](int2 r, int ord0) {  // {tma row or -1, page_info}
     const int cnt = warp_count(r);
     for (int j = lane; j < cnt; j += 32) {
       const int64_t x = (int64_t)r.x + warp + (int64_t)NW * j;
@@ -281,13 +317,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const int np = pfx[b + 1] - pfx[b];
       const int64_t rr = x - (int64_t)p.Hkv * pfx[b];
       const int h = (int)(rr / np);
-      const int pg = (int)(rr - (int64_t)h * np);
+      const int pgu = (int)(rr - (int64_t)h * np);  // unit within the segment
+      const int pg = pgu < gns[b] ? pgu : pgu + gsk[b];
       const int blk = p.block_tables[(int64_t)b * p.MBS + pg];
       int row = -1;
       if (blk >= 0 && blk < p.NB) row = (blk * p.Hkv + h) * kPageSize;
       else report_error(p.err_word, PKV_ERR_BOUNDS);
-      desc[(ord0 + j) % kDescRing] = make_int2(row, min(kRemCap, ctxs[b] - pg * kPageSize));
-      if (j == 0 || pg == 0) {  // a segment may start here: warm its q rows in L2
+      desc[(ord0 + j) % kDescRing] = make_int2(row, page_info(b, pg));
+      if (j == 0 || pgu == 0) {  // a segment may start here: warm its q rows in L2
         for (int i = 0; i < p.qlen; ++i) {
           const char* qp = reinterpret_cast<const char*>(p.q) +
                            (((int64_t)b * p.qlen + i) * p.Hq + h * G) * D * 2;
@@ -314,10 +351,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const int np = pfx[b + 1] - pfx[b];
       const int64_t rr = x - (int64_t)p.Hkv * pfx[b];
       f_h = (int)(rr / np);
-      const int pg = (int)(rr - (int64_t)f_h * np);
+      const int pgu = (int)(rr - (int64_t)f_h * np);  // unit within the segment
+      const int pg = pgu < gns[b] ? pgu : pgu + gsk[b];
       f_blk = p.block_tables[(int64_t)b * p.MBS + pg];
-      f_valid = min(kRemCap, ctxs[b] - pg * kPageSize);
-      if (lane == 0 || pg == 0) {  // a segment may start here: warm its q rows in L2
+      f_valid = page_info(b, pg);
+      if (lane == 0 || pgu == 0) {  // a segment may start here: warm its q rows in L2
         for (int i = 0; i < p.qlen; ++i) {
           const char* qp = reinterpret_cast<const char*>(p.q) +
                            (((int64_t)b * p.qlen + i) * p.Hq + f_h * G) * D * 2;
@@ -556,7 +594,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const int rem = valids[i];  // tokens from the page's start to the context's end
+      const int v = valids[i];
+      const int rem = v & kRemMask;  // tokens from the page's start to the context's end
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[i][e] *= c2;
       if constexpr (QC == 1) {
@@ -564,16 +603,31 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
           if (r8 >= rem) x[i][0] = x[i][1] = -INFINITY;
           if (r8 + 8 >= rem) x[i][2] = x[i][3] = -INFINITY;
         }
-      } else if (rem < kPageSize + QC - 1) {
-        // causal among the new tokens: query token j of the last qlen sees
-        // the page's first rem - (qlen - 1 - j) tokens
+        if (v & kWinFlag) {  // rows before the window's start that are no sinks
+          const int sr = (v >> 6) & 15, wr = ((v >> 11) & 63) - 8;
+          if (r8 < wr && r8 >= sr) x[i][0] = x[i][1] = -INFINITY;
+          if (r8 + 8 < wr && r8 + 8 >= sr) x[i][2] = x[i][3] = -INFINITY;
+        }
+      } else {
         const int c0 = 2 * c4, c1 = 2 * c4 + 1;
-        const int l0 = col_real(c0) ? rem - (p.qlen - 1 - c0 / G) : rem;
-        const int l1 = col_real(c1) ? rem - (p.qlen - 1 - c1 / G) : rem;
-        if (r8 >= l0) x[i][0] = -INFINITY;
-        if (r8 >= l1) x[i][1] = -INFINITY;
-        if (r8 + 8 >= l0) x[i][2] = -INFINITY;
-        if (r8 + 8 >= l1) x[i][3] = -INFINITY;
+        const int j0 = col_real(c0) ? c0 / G : p.qlen - 1, j1 = col_real(c1) ? c1 / G : p.qlen - 1;
+        if (rem < kPageSize + QC - 1) {
+          // causal among the new tokens: query token j of the last qlen sees
+          // the page's first rem - (qlen - 1 - j) tokens
+          const int l0 = rem - (p.qlen - 1 - j0), l1 = rem - (p.qlen - 1 - j1);
+          if (r8 >= l0) x[i][0] = -INFINITY;
+          if (r8 >= l1) x[i][1] = -INFINITY;
+          if (r8 + 8 >= l0) x[i][2] = -INFINITY;
+          if (r8 + 8 >= l1) x[i][3] = -INFINITY;
+        }
+        if (v & kWinFlag) {  // query token j's window starts j rows after token 0's
+          const int sr = (v >> 6) & 15, wr = ((v >> 11) & 63) - 8;
+          const int w0 = wr + j0, w1 = wr + j1;
+          if (r8 < w0 && r8 >= sr) x[i][0] = -INFINITY;
+          if (r8 < w1 && r8 >= sr) x[i][1] = -INFINITY;
+          if (r8 + 8 < w0 && r8 + 8 >= sr) x[i][2] = -INFINITY;
+          if (r8 + 8 < w1 && r8 + 8 >= sr) x[i][3] = -INFINITY;
+        }
       }
       mx0 = fmaxf(mx0, fmaxf(x[i][0], x[i][2]));
       mx1 = fmaxf(mx1, fmaxf(x[i][1], x[i][3]));
@@ -621,7 +675,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const float2 f01 = unpack2<kBF>(h01), f23 = unpack2<kBF>(h23);
       const uint32_t l01 = pack2<kBF>(p0 - f01.x, p1 - f01.y);
       const uint32_t l23 = pack2<kBF>(p2 - f23.x, p3 - f23.y);
-      pv_page(kt[i] + C::kTileBytes, valids[i] < kPageSize ? valids[i] : kPageSize, movm_trans(h01),
+      const int vrows = valids[i] & kRemMask;
+      pv_page(kt[i] + C::kTileBytes, vrows < kPageSize ? vrows : kPageSize, movm_trans(h01),
               movm_trans(h23), movm_trans(l01), movm_trans(l23));
     }
   };

@@ -42,7 +42,7 @@ constexpr int decode_fixed_smem(int d) {
 constexpr int kDecodeSmemTarget = 113 * 1024;
 constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
 constexpr int decode_stages(int d, CacheKind c) {
-  return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d) - 1560) /
+  return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d) - 2600) /
                              (kDecodeWarps * decode_stage_bytes(d, c)));
 }
 
@@ -62,6 +62,8 @@ struct DecodeParams {
   int32_t B, Hq, Hkv, d, NB, MBS;
   pkv_dtype out_dtype;
   int32_t qlen;                // query tokens per sequence (q, out are [B][qlen][Hq][d])
+  int32_t window;              // > 0: query at position t sees t - window + 1 .. t (and sinks)
+  int32_t sinks;               // with a window: positions 0 .. sinks - 1 stay visible
   int32_t early_prologue;      // 1: read lengths/tables before waiting on the previous kernel
   float scale_log2;            // softmax scale * log2(e)
 };
@@ -94,7 +96,7 @@ struct AppendParams {
 inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
   return (size_t)decode_fixed_smem(d) +
          (size_t)kDecodeWarps * decode_stages(d, cache) * decode_stage_bytes(d, cache) +
-         (size_t)(3 * B + 2) * 4;
+         (size_t)(5 * B + 2) * 4;
 }
 
 // Returns a CUDA error (cudaSuccess when the kernel was enqueued) or
