@@ -10,6 +10,9 @@
  *      (1,N) attention row over the cached keys and values, read through the
  *      sequence's block table.
  *
+ * pkv_decode_step validates and enqueues both; pkv_decode_step_fused does
+ * both in one kernel, each new row going to its sequence's newest position.
+ *
  * Sources (web pages):
  *   [KVFA] "KV Cache & Flash Attention." (kvcache-7e2.pages.dev)
  *   [DF]   "KV Cache & FlashAttention" (deepforge.srivtx.xyz)
@@ -87,6 +90,9 @@ typedef struct {
   const float* v_scale;  /* device fp32 [Hkv]; FP8 only                     */
   int32_t* err_word;     /* optional device int32; NULL = do not report    */
 } pkv_cache_desc;
+
+/* Flags of pkv_decode_step_fused. */
+#define PKV_STEP_OVERLAP 1
 
 /* Append (scatter) new K/V rows into their cache slots.
  * [KVFA] KV-cache section (append one K and one V per token) and
@@ -219,6 +225,42 @@ PKV_API pkv_status pkv_decode_step(
     int32_t max_blocks_per_seq, int32_t max_context_len_hint, float scale,
     void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
     size_t workspace_bytes, pkv_stream_t stream);
+
+/* One decode step in ONE kernel: pkv_decode_step with each sequence's new
+ * token placed at its position context_lens[b] - 1, i.e. in block
+ * block_tables[b][(context_lens[b] - 1) / P] at offset (context_lens[b] - 1)
+ * % P ([KVFA] KV-cache section: append, then attend over all tokens;
+ * PagedAttention section: position -> (block, offset)).  With a 16-bit
+ * cache the warp that stages that page writes the new K and V row into its
+ * staged copy, which this pass attends to, and into the cache, for later
+ * steps: one launch, no slot mapping.  With an E4M3 cache the call enqueues
+ * two kernels: the append (each row to its sequence's newest position,
+ * encoded as pkv_kv_append encodes it), then the attention overlapping its
+ * tail.  Either way the cache bytes are those pkv_kv_append writes.
+ *   k, v          [batch][num_kv_heads][head_dim] of kv_dtype (F16 or BF16;
+ *                 for 16-bit caches it must equal cache_dtype).  A sequence
+ *                 with context_lens[b] == 0 appends nothing.
+ *   flags         0, or PKV_STEP_OVERLAP: context_lens and block_tables are
+ *                 not written by the kernel launched just before this call
+ *                 on the stream (host copies and earlier kernels may write
+ *                 them).  The kernel then reads them, and lays out its work,
+ *                 while that kernel finishes (programmatic dependent
+ *                 launch), and lets the next kernel on the stream launch
+ *                 before it ends (a programmatic dependent must wait for it
+ *                 before reading its outputs, as that launch mode requires).
+ *                 Every other input is read after the preceding kernel
+ *                 completes.  Without the flag every input is.  Other bits
+ *                 return PKV_ERR_INVALID_ARG.
+ * The block receiving a new row must not be read at that row by another
+ * sequence of the same call (copy it first: pkv_copy_blocks).  Other
+ * arguments and guarantees as for pkv_paged_decode_attention. */
+PKV_API pkv_status pkv_decode_step_fused(
+    const pkv_cache_desc* desc, const void* q, void* k_cache, void* v_cache,
+    const void* k, const void* v, pkv_dtype kv_dtype,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t batch,
+    int32_t max_blocks_per_seq, int32_t max_context_len_hint, float scale,
+    void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
+    size_t workspace_bytes, int32_t flags, pkv_stream_t stream);
 
 /* Size of the fixed device scratch behind pkv_paged_decode_attention_noalloc
  * (32 MiB, held by every GPU that loads the library until the process ends). */

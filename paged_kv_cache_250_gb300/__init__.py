@@ -12,6 +12,8 @@ memory and streams.  The functions carry the C names:
                                   attention sinks
     pkv_decode_step               both, validated together, the attention
                                   kernel overlapping the append's tail
+    pkv_decode_step_fused         both in one kernel (new token at its
+                                  sequence's newest position)
     pkv_copy_blocks               copy whole blocks (copy-on-write of a
                                   shared prefix's last block)
     pkv_paged_decode_attention_noalloc  decode without a caller workspace
@@ -39,20 +41,22 @@ __all__ = [
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES", "pkv_copy_blocks",
     "pkv_paged_decode_attention_multi", "pkv_paged_decode_attention_window",
+    "pkv_decode_step_fused",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
-    "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "EXPORTED_SYMBOLS",
+    "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "PKV_STEP_OVERLAP", "EXPORTED_SYMBOLS",
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE = 0, 1, 2, 3
 PKV_ERR_CUDA, PKV_ERR_BOUNDS, PKV_ERR_TIMEOUT = 4, 5, 6
 PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
+PKV_STEP_OVERLAP = 1
 
 EXPORTED_SYMBOLS = (
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "pkv_copy_blocks", "pkv_paged_decode_attention_multi",
-    "pkv_paged_decode_attention_window",
+    "pkv_paged_decode_attention_window", "pkv_decode_step_fused",
 )
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -118,6 +122,9 @@ def load_library():
         lib.pkv_paged_decode_attention_multi.restype = I32
         lib.pkv_paged_decode_attention_multi.argtypes = [D, P, P, P, P, P, I32, I32, I32, I32,
                                                          ctypes.c_float, P, I32, I32, P, SZ, P]
+        lib.pkv_decode_step_fused.restype = I32
+        lib.pkv_decode_step_fused.argtypes = [D, P, P, P, P, P, I32, P, P, I32, I32, I32,
+                                              ctypes.c_float, P, I32, I32, P, SZ, I32, P]
         lib.pkv_paged_decode_attention_window.restype = I32
         lib.pkv_paged_decode_attention_window.argtypes = [D, P, P, P, P, P, I32, I32, I32, I32,
                                                           I32, I32, ctypes.c_float, P, I32, I32,
@@ -311,6 +318,34 @@ def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _stream_handle(stream, q.device))
     _check(st, "pkv_decode_step")
+
+
+def pkv_decode_step_fused(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                          out: torch.Tensor, workspace: torch.Tensor,
+                          max_context_len_hint: int = 0, stream=None,
+                          overlap: bool = False) -> None:
+    """One kernel: sequence b's new token (k[b], v[b]: [B][Hkv][d]) goes to its
+    position context_lens[b] - 1, then every sequence attends.  overlap sets
+    PKV_STEP_OVERLAP: context_lens and block_tables are not written by the
+    kernel launched just before on the stream."""
+    lib = load_library()
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    B, mbs = int(block_tables.shape[0]), int(block_tables.shape[1])
+    if k.shape[0] != B or v.shape != k.shape:
+        raise ValueError("k and v need one row per sequence")
+    st = lib.pkv_decode_step_fused(
+        ctypes.byref(desc), _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+        _DTYPE_CODE.get(k.dtype, -1), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(context_lens, "context_lens"), B, mbs, int(max_context_len_hint),
+        float(scale), _dev_ptr(out, "out"), _DTYPE_CODE.get(q.dtype, -1),
+        _DTYPE_CODE.get(out.dtype, -1), _dev_ptr(workspace, "workspace"),
+        int(workspace.numel() * workspace.element_size()), PKV_STEP_OVERLAP if overlap else 0,
+        _stream_handle(stream, q.device))
+    _check(st, "pkv_decode_step_fused")
 
 
 def pkv_paged_decode_attention_noalloc(desc: CacheDesc, q: torch.Tensor,

@@ -214,7 +214,9 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
                        int32_t max_context_len_hint, float scale, void* out, pkv_dtype q_dtype,
                        pkv_dtype out_dtype, void* workspace, size_t workspace_bytes,
                        pkv_stream_t stream, int early_prologue, int32_t qlen = 1,
-                       int32_t window = 0, int32_t sinks = 0) {
+                       int32_t window = 0, int32_t sinks = 0, const void* k_new = nullptr,
+                       const void* v_new = nullptr, pkv_dtype kv_dtype = PKV_BF16,
+                       int trigger_next = 0) {
   pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                                 max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
                                 out_dtype, workspace, workspace_bytes);
@@ -245,8 +247,14 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
   l.p.MBS = max_blocks_per_seq;
   l.p.out_dtype = out_dtype;
   l.p.early_prologue = early_prologue;
+  l.p.trigger_next = trigger_next;
   l.p.qlen = qlen;
   l.p.window = window;
+  l.p.k_new = k_new;
+  l.p.v_new = v_new;
+  l.p.k_cache = const_cast<void*>(k_cache);
+  l.p.v_cache = const_cast<void*>(v_cache);
+  l.p.kv_bf16 = kv_dtype == PKV_BF16 ? 1 : 0;
   l.p.sinks = window > 0 ? sinks : 0;
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.group = desc->num_q_heads / desc->num_kv_heads;
@@ -296,6 +304,9 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.slot_mapping = slot_mapping;
+  a.block_tables = nullptr;
+  a.context_lens = nullptr;
+  a.MBS = 0;
   a.k = k;
   a.v = v;
   a.k_scale = desc->k_scale;
@@ -407,6 +418,58 @@ pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, void* k_ca
   return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                      max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
                      workspace, workspace_bytes, stream, /*early_prologue=*/1);
+}
+
+pkv_status pkv_decode_step_fused(const pkv_cache_desc* desc, const void* q, void* k_cache,
+                                 void* v_cache, const void* k, const void* v,
+                                 pkv_dtype kv_dtype, const int32_t* block_tables,
+                                 const int32_t* context_lens, int32_t batch,
+                                 int32_t max_blocks_per_seq, int32_t max_context_len_hint,
+                                 float scale, void* out, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                                 void* workspace, size_t workspace_bytes, int32_t flags,
+                                 pkv_stream_t stream) {
+  pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                                max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
+                                out_dtype, workspace, workspace_bytes);
+  if (st != PKV_OK || batch == 0) return st;
+  if (!k || !v) return PKV_ERR_INVALID_ARG;
+  if (kv_dtype != PKV_F16 && kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (desc->cache_dtype != PKV_FP8_E4M3 && kv_dtype != desc->cache_dtype)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16)) return PKV_ERR_INVALID_ARG;
+  if ((flags & ~PKV_STEP_OVERLAP) != 0) return PKV_ERR_INVALID_ARG;
+  const int overlap = (flags & PKV_STEP_OVERLAP) ? 1 : 0;
+  if (desc->cache_dtype == PKV_FP8_E4M3) {
+    // E4M3: the append kernel (each sequence's newest position, from its
+    // table), then the attention overlapping its tail
+    pkv::AppendParams a;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.slot_mapping = nullptr;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.MBS = max_blocks_per_seq;
+    a.k = k;
+    a.v = v;
+    a.k_scale = desc->k_scale;
+    a.v_scale = desc->v_scale;
+    a.err_word = desc->err_word;
+    a.T = batch;
+    a.Hkv = desc->num_kv_heads;
+    a.d = desc->head_dim;
+    a.NB = desc->num_blocks;
+    if (pkv::launch_append(a, pkv::kCacheE4M3, kv_dtype == PKV_BF16,
+                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                       max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                       workspace, workspace_bytes, stream, /*early_prologue=*/1, 1, 0, 0,
+                       nullptr, nullptr, kv_dtype, /*trigger_next=*/overlap);
+  }
+  return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                     max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                     workspace, workspace_bytes, stream, /*early_prologue=*/overlap, 1, 0, 0, k,
+                     v, kv_dtype, /*trigger_next=*/overlap);
 }
 
 uint64_t pkv_kv_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim,

@@ -14,21 +14,6 @@ namespace pkv {
 // skipped; slots past the pool are reported, never written.  For an E4M3
 // cache each value is divided by its head's scale (IEEE fp32) and encoded
 // round-to-nearest-even with saturation to +-448.
-template <bool IN_BF16>
-__device__ __forceinline__ uint2 quantize8(uint4 in, float scale) {
-  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-  uint32_t outw[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float2 a = unpack2<IN_BF16>(w[2 * i]);
-    const float2 b = unpack2<IN_BF16>(w[2 * i + 1]);
-    const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
-    const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale));
-    outw[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-  }
-  return make_uint2(outw[0], outw[1]);
-}
-
 template <int CACHE, bool IN_BF16>
 __global__ void append_kernel(const AppendParams a) {
   // let a dependent decode kernel start its prologue while this one runs
@@ -40,7 +25,16 @@ __global__ void append_kernel(const AppendParams a) {
   const int part = (int)(tid - row * per_row);
   const int t = (int)(row / a.Hkv);
   const int h = (int)(row - (int64_t)t * a.Hkv);
-  const int64_t slot = a.slot_mapping[t];
+  int64_t slot;
+  if (a.slot_mapping != nullptr) {
+    slot = a.slot_mapping[t];
+  } else {  // the newest position of sequence t (none when it is empty)
+    const int c = a.context_lens[t];
+    if (c <= 0 || c > a.MBS * kPageSize) return;  // lengths are checked by the attention
+    const int blk = a.block_tables[(int64_t)t * a.MBS + (c - 1) / kPageSize];
+    if (blk < 0 || blk >= a.NB) return;  // reported by the attention's own lookup
+    slot = (int64_t)blk * kPageSize + (c - 1) % kPageSize;
+  }
   if (slot < 0) return;
   if (slot >= (int64_t)a.NB * kPageSize) {
     if (part == 0) report_error(a.err_word, PKV_ERR_BOUNDS);

@@ -147,7 +147,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   // pages a warp takes per step: 2 on rings of 3+ pages (4 measured slower:
   // longer P.V accumulation chains)
   constexpr int kGroup = kS >= 3 ? 2 : 1;
+  // the one-kernel step writes new rows in the main loop for 16-bit caches
+  // only (E4M3 steps enqueue the append kernel first)
+  constexpr bool kFusedAppend = QC == 1 && CACHE != kCacheE4M3;
 
+  // the next kernel on the stream may launch (a programmatic dependent waits
+  // for this one to complete before it reads what this one writes)
+  if (p.trigger_next) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!p.early_prologue) griddep_wait();
 
   extern __shared__ uint8_t smem_raw[];
@@ -686,6 +692,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     compute_pages(Int<1>{}, kt1, v1);
   };
 
+  // ---- fused append (16-bit caches): the page holding a sequence's newest
+  // position gets that token's K and V row from the step's inputs, in the
+  // staged copy (so this pass attends to it) and in the cache (for later
+  // steps).  The page (b, h) is staged by this warp alone, so nothing else in
+  // the grid reads the row.
+  auto append_new = [&](uint32_t kt, int tma_row, int r, int b, int h) {
+    if (lane < D / 8) {  // 8 elements (16 bytes) per lane
+      const int64_t src = ((int64_t)b * p.Hkv + h) * (D / 8) + lane;
+      const uint4 kin = reinterpret_cast<const uint4*>(p.k_new)[src];
+      const uint4 vin = reinterpret_cast<const uint4*>(p.v_new)[src];
+      const int64_t dst = ((int64_t)tma_row + r) * (D / 8) + lane;
+      reinterpret_cast<uint4*>(p.k_cache)[dst] = kin;
+      reinterpret_cast<uint4*>(p.v_cache)[dst] = vin;
+      const uint32_t off = swz(r, lane);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kt + off), "r"(kin.x),
+                   "r"(kin.y), "r"(kin.z), "r"(kin.w) : "memory");
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kt + C::kTileBytes + off),
+                   "r"(vin.x), "r"(vin.y), "r"(vin.z), "r"(vin.w) : "memory");
+      // the slot is refilled by the tensor-copy (async) proxy later
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+  };
+
   // ---- merging warp states through shared memory: element i of the lane
   // state (m[2], l[2], o[MT][4]) at buf[i * S + li]
   auto store_state_at = [&](float* buf, int li, int S) {
@@ -1014,7 +1044,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
           const int ng = (j1 - j >= kGroup) ? kGroup : 1;
           if (ng > 1) {
             uint32_t kt[kGroup];
-            int vv[kGroup];
+            int vv[kGroup], rw[kGroup];
             bool all_ok = true;
 #pragma unroll
             for (int i = 0; i < kGroup; ++i) {
@@ -1026,7 +1056,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                   set_dead(k + i);
                 kt[i] = ring + (uint32_t)(si * C::kStageBytes);
                 vv[i] = (di.x >= 0) ? di.y : 0;
+                rw[i] = di.x;
                 all_ok = all_ok && vv[i] > 0;
+              }
+            }
+            if constexpr (kFusedAppend) {
+              if (p.k_new != nullptr && !dead) {
+#pragma unroll
+                for (int i = 0; i < kGroup; ++i)  // rem <= P: the page with the newest token
+                  if (i < ng && vv[i] > 0 && (vv[i] & kRemMask) <= kPageSize)
+                    append_new(kt[i], rw[i], (vv[i] & kRemMask) - 1, b, h);
               }
             }
             if (!dead) {
@@ -1050,6 +1089,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         if (!dead && !mbar_wait_bounded(smem_u32(&bars[warp * kS + slot]),
                                         (uint32_t)((k / kS) & 1), kWaitLimitNs))
           set_dead(k);
+        if constexpr (kFusedAppend) {
+          if (p.k_new != nullptr && !dead && dsc.x >= 0 && dsc.y > 0 &&
+              (dsc.y & kRemMask) <= kPageSize)
+            append_new(ring + (uint32_t)(slot * C::kStageBytes), dsc.x, (dsc.y & kRemMask) - 1,
+                       b, h);
+        }
         if (!dead && dsc.x >= 0 && dsc.y > 0)
           compute_page(ring + (uint32_t)(slot * C::kStageBytes), dsc.y);
         __syncwarp();

@@ -170,4 +170,21 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return d;
 }
 
+// Eight 16-bit values (one uint4) -> eight E4M3 bytes: each divided by
+// `scale` in IEEE fp32, then encoded round-to-nearest-even with saturation.
+template <bool IN_BF16>
+__device__ __forceinline__ uint2 quantize8(uint4 in, float scale) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t outw[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 a = unpack2<IN_BF16>(w[2 * i]);
+    const float2 b = unpack2<IN_BF16>(w[2 * i + 1]);
+    const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
+    const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale));
+    outw[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return make_uint2(outw[0], outw[1]);
+}
+
 }  // namespace pkv

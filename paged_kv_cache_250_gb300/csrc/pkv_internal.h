@@ -62,9 +62,15 @@ struct DecodeParams {
   int32_t B, Hq, Hkv, d, NB, MBS;
   pkv_dtype out_dtype;
   int32_t qlen;                // query tokens per sequence (q, out are [B][qlen][Hq][d])
+  const void* k_new;           // fused append: new K rows [B][Hkv][d] (NULL: none)
+  const void* v_new;           // fused append: new V rows
+  void* k_cache;               // fused append: the caches those rows are written into
+  void* v_cache;
+  int32_t kv_bf16;             // fused append: k_new / v_new are bf16 (else fp16)
   int32_t window;              // > 0: query at position t sees t - window + 1 .. t (and sinks)
   int32_t sinks;               // with a window: positions 0 .. sinks - 1 stay visible
   int32_t early_prologue;      // 1: read lengths/tables before waiting on the previous kernel
+  int32_t trigger_next;        // 1: let the next kernel on the stream launch at once
   float scale_log2;            // softmax scale * log2(e)
 };
 
@@ -83,7 +89,10 @@ struct DecodeLaunch {
 struct AppendParams {
   void* k_cache;
   void* v_cache;
-  const int64_t* slot_mapping;
+  const int64_t* slot_mapping;   // NULL: token t goes to position context_lens[t] - 1
+  const int32_t* block_tables;   // of sequence t, through its block table
+  const int32_t* context_lens;
+  int32_t MBS;
   const void* k;
   const void* v;
   const float* k_scale;

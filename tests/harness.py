@@ -136,6 +136,17 @@ class GpuRun:
                             out, self.workspace, self.hint)
         return out
 
+    def step_one_kernel(self, out_dtype: str = "f32") -> torch.Tensor:
+        """One decode step as a single kernel (pkv_decode_step_fused): each new
+        row lands at its sequence's newest position."""
+        cfg = self.w.cfg
+        out = torch.empty(cfg.batch, cfg.q_heads, cfg.head_dim, dtype=_DT[out_dtype],
+                          device=self.dev)
+        pkv.pkv_decode_step_fused(self.desc, self.q, self.k_cache, self.v_cache, self.k_new,
+                                  self.v_new, self.tables, self.ctx, cfg.softmax_scale, out,
+                                  self.workspace, self.hint)
+        return out
+
     def err_code(self) -> int:
         return 0 if self.err is None else int(self.err.item())
 
