@@ -8,8 +8,9 @@ numpy marshalling below.
 
 What it computes, and where each definition comes from, is stated beside each
 function in ``pkv_oracle.c``.  Every function here is pinned by the
-``-m "not gpu"`` tests in ``tests/test_oracle_pins.py`` against values the
-pages print, closed forms, special cases and library routines.
+``-m "not gpu"`` tests (``tests/test_oracle_pins.py`` and the ``*_oracle.py``
+files beside it) against values the pages print, closed forms, special cases
+and library routines.
 """
 from __future__ import annotations
 
@@ -88,6 +89,12 @@ def _load():
         lib.pkvo_append_bytes.argtypes = [P, P, P, I32, I32, I32, I32, I32, I32]
         lib.pkvo_append_e4m3.restype = None
         lib.pkvo_append_e4m3.argtypes = [P, P, P, P, I32, I32, I32, I32, I32]
+        lib.pkvo_e4m3_token_scale.restype = ctypes.c_float
+        lib.pkvo_e4m3_token_scale.argtypes = [P, I32]
+        lib.pkvo_append_e4m3_token.restype = None
+        lib.pkvo_append_e4m3_token.argtypes = [P, P, P, P, I32, I32, I32, I32, I32]
+        lib.pkvo_e4m3_dequantize_rows.restype = None
+        lib.pkvo_e4m3_dequantize_rows.argtypes = [P, P, I64, I32, P]
         lib.pkvo_copy_blocks.restype = None
         lib.pkvo_copy_blocks.argtypes = [P, P, P, I32, I32, I64]
         _lib = lib
@@ -147,6 +154,23 @@ def e4m3_dequantize(codes, scale: float) -> np.ndarray:
     out = np.empty(c.shape, dtype=np.float64)
     _load().pkvo_e4m3_dequantize_array(_ptr(c), c.size,
                                        float(np.float32(scale)), _ptr(out))
+    return out
+
+
+def e4m3_token_scale(row) -> float:
+    """Per-token FP8 scale of one (token, KV head) row: its largest magnitude
+    over 448 in IEEE fp32 (1 for an all-zero row)."""
+    r = np.ascontiguousarray(np.asarray(row, dtype=np.float32).reshape(-1))
+    return float(_load().pkvo_e4m3_token_scale(_ptr(r), r.size))
+
+
+def e4m3_dequantize_rows(codes, row_scale) -> np.ndarray:
+    """fp64 rows [n][d] of E4M3 codes, each times its own fp32 scale."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    n, d = c.shape
+    rs = np.ascontiguousarray(np.asarray(row_scale, dtype=np.float32).reshape(n))
+    out = np.empty((n, d), dtype=np.float64)
+    _load().pkvo_e4m3_dequantize_rows(_ptr(c), _ptr(rs), n, d, _ptr(out))
     return out
 
 
@@ -245,6 +269,19 @@ def append_e4m3(cache: np.ndarray, src, slot, head_scale) -> np.ndarray:
     _load().pkvo_append_e4m3(_ptr(out), _ptr(srcf), _ptr(slot), _ptr(hs),
                              slot.size, NB, P, Hkv, d)
     return out
+
+
+def append_e4m3_token(cache: np.ndarray, scales: np.ndarray, src, slot):
+    """Expected per-token E4M3 cache [NB][Hkv][P][d] and scale pool
+    [NB][Hkv][P] after an append of fp32-valued rows ``src`` [T][Hkv][d]."""
+    out = np.ascontiguousarray(cache, dtype=np.uint8).copy()
+    sc = np.ascontiguousarray(scales, dtype=np.float32).copy()
+    srcf = np.ascontiguousarray(np.asarray(src, dtype=np.float32))
+    NB, Hkv, P, d = out.shape
+    slot = np.ascontiguousarray(np.asarray(slot, dtype=np.int64))
+    _load().pkvo_append_e4m3_token(_ptr(out), _ptr(sc), _ptr(srcf), _ptr(slot), slot.size,
+                                   NB, P, Hkv, d)
+    return out, sc
 
 
 def copy_blocks(cache: np.ndarray, src, dst) -> np.ndarray:

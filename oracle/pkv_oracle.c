@@ -329,6 +329,51 @@ void pkvo_copy_blocks(uint8_t* cache, const int32_t* src, const int32_t* dst, in
   }
 }
 
+/* Per-token FP8 scaling ("KV Cache & Flash Attention." (kvcache-7e2.pages.dev),
+ * memory-cost section: the cache is quantized to fp8; Flash Attention
+ * section: FP8 with finer-grained, per-block scales).  Reading: every appended
+ * (token, KV head) row of K, and of V, gets its own fp32 scale, the row's
+ * largest magnitude divided by 448 (the largest finite E4M3 value) in IEEE
+ * fp32, so the row's largest element lands on +-448; an all-zero row takes
+ * scale 1.  The row is then encoded under that scale like any E4M3 value. */
+float pkvo_e4m3_token_scale(const float* row, int32_t d) {
+  float amax = 0.0f;
+  for (int32_t j = 0; j < d; ++j) {
+    const float a = fabsf(row[j]);
+    if (a > amax) amax = a;
+  }
+  if (amax == 0.0f) return 1.0f;
+  volatile float s = amax / 448.0f;
+  return s;
+}
+
+/* Per-token FP8 append: codes into the cache slot, the row's scale into the
+ * same slot of the scale pool [NB][Hkv][P]. */
+void pkvo_append_e4m3_token(uint8_t* cache, float* scales, const float* src,
+                            const int64_t* slot, int32_t T, int32_t NB, int32_t P,
+                            int32_t Hkv, int32_t d) {
+  for (int32_t t = 0; t < T; ++t) {
+    if (slot[t] < 0) continue;
+    int64_t blk = slot[t] / P, off = slot[t] % P;
+    if (blk >= NB) continue;
+    for (int32_t h = 0; h < Hkv; ++h) {
+      const int64_t r = (blk * Hkv + h) * P + off;
+      const float* s = src + ((int64_t)t * Hkv + h) * d;
+      const float sc = pkvo_e4m3_token_scale(s, d);
+      scales[r] = sc;
+      for (int32_t j = 0; j < d; ++j) cache[r * d + j] = pkvo_e4m3_quantize(s[j], sc);
+    }
+  }
+}
+
+/* fp64 rows [n][d] from codes and one fp32 scale per row. */
+void pkvo_e4m3_dequantize_rows(const uint8_t* codes, const float* row_scale, int64_t n,
+                               int32_t d, double* out) {
+  for (int64_t i = 0; i < n; ++i)
+    for (int32_t j = 0; j < d; ++j)
+      out[i * d + j] = pkvo_e4m3_decode(codes[i * d + j]) * (double)row_scale[i];
+}
+
 /* FP8 cache: the row is divided by the KV head's fp32 scale and encoded. */
 void pkvo_append_e4m3(uint8_t* cache, const float* src, const int64_t* slot,
                       const float* head_scale, int32_t T, int32_t NB, int32_t P,
