@@ -47,7 +47,8 @@ DEFAULT_CONFIG = "llama3_8b_b32_ctx1-4096_bf16"
 METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and tokens/s per layer"
 L2_BYTES = 129 * 1024 * 1024
 PEAK_FALLBACK_GBS = 6800.0
-_CODE = {"f16": pkv.PKV_F16, "bf16": pkv.PKV_BF16, "e4m3": pkv.PKV_FP8_E4M3}
+_CODE = {"f16": pkv.PKV_F16, "bf16": pkv.PKV_BF16, "e4m3": pkv.PKV_FP8_E4M3,
+         "e4m3tok": pkv.PKV_FP8_E4M3_TOKEN}
 _DT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -164,6 +165,9 @@ def algorithmic_bytes(cfg, ctx: torch.Tensor):
     if cfg.cache == "e4m3":
         attn += 8 * Hkv
     append = B * Hkv * d * 2 * (2 + e_c) + 8 * B
+    if cfg.cache == "e4m3tok":  # a K and a V scale per token and KV head, read and written
+        attn += int(ctx64.sum()) * Hkv * 8
+        append += B * Hkv * 8
     return attn, append
 
 
@@ -353,7 +357,7 @@ def run_native(args, cfg, rank, world, device):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[cfg.cache],
+        "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3", "e4m3tok": "e4m3"}[cfg.cache],
         "data": "synthetic (seeded N(0,1) q/k/v, uniform ragged context lengths, "
                 "permuted block tables)",
         "config": {**workload_config(cfg, st.w.ctx),
@@ -615,7 +619,7 @@ def run_multi_query(args, cfg, device, windowed: bool = False):
     return {"metric": f"{what} decode-attention achieved HBM GB/s", "value": round(value, 1),
             "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[cfg.cache],
+            "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3", "e4m3tok": "e4m3"}[cfg.cache],
             "data": "synthetic (seeded N(0,1) q/k/v, the workload's lengths and tables)",
             "config": {**workload_config(cfg, st.w.ctx), **extra,
                        "tokens_per_s_per_layer": round(cfg.batch * qlen / (ms * 1e-3), 1),

@@ -71,7 +71,8 @@ typedef enum {
   PKV_F16 = 0,
   PKV_BF16 = 1,
   PKV_FP8_E4M3 = 2, /* OCP E4M3 (bias 7, max 448, no infinities)         */
-  PKV_F32 = 3
+  PKV_F32 = 3,
+  PKV_FP8_E4M3_TOKEN = 4 /* E4M3 cache, one fp32 scale per token and head  */
 } pkv_dtype;
 
 /* Shape of the paged cache, shared by both calls.
@@ -86,8 +87,14 @@ typedef struct {
   int32_t num_q_heads;   /* Hq, a multiple of Hkv                          */
   int32_t head_dim;      /* d                                              */
   pkv_dtype cache_dtype; /* F16 | BF16 | FP8_E4M3                          */
-  const float* k_scale;  /* device fp32 [Hkv]; FP8 only: stored K = k/scale */
-  const float* v_scale;  /* device fp32 [Hkv]; FP8 only                     */
+  const float* k_scale;  /* FP8_E4M3: device fp32 [Hkv], stored K = k/scale.
+                            FP8_E4M3_TOKEN: the scale pool, device fp32
+                            [NB][Hkv][2][P], 128-byte aligned: for each
+                            (block, KV head) the P slots' K scales, then
+                            their V scales; written by the append.
+                            NULL for 16-bit caches.                        */
+  const float* v_scale;  /* FP8_E4M3: device fp32 [Hkv] for V; unused
+                            otherwise                                       */
   int32_t* err_word;     /* optional device int32; NULL = do not report    */
 } pkv_cache_desc;
 
@@ -105,6 +112,13 @@ typedef struct {
  *                BF16; for 16-bit caches it must equal cache_dtype).
  *   For FP8_E4M3 caches each element is divided by its head's scale in IEEE
  *   fp32 and encoded round-to-nearest-even with saturation to +-448.
+ *   For FP8_E4M3_TOKEN caches each (token, KV head) row of K, and of V, gets
+ *   its own scale, the row's largest magnitude divided by 448 in IEEE fp32
+ *   (1 for an all-zero row), written to the slot's K (or V) entry of the
+ *   scale pool;
+ *   the row is then encoded under it as above ([KVFA] memory-cost section:
+ *   the cache is quantized to fp8; Flash Attention section: FP8 with finer-
+ *   grained scales).  head_dim 128.
  *   Slots written by two tokens of one call race; the caller avoids it. */
 PKV_API pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache,
                          void* v_cache, const int64_t* slot_mapping,
@@ -176,6 +190,7 @@ PKV_API pkv_status pkv_paged_decode_attention(
  *   q, out        [batch][q_len][num_q_heads][head_dim].
  *   q_len         1 .. 8 / (num_q_heads / num_kv_heads); larger returns
  *                 PKV_ERR_UNSUPPORTED.  q_len 1 is pkv_paged_decode_attention.
+ *                 FP8_E4M3_TOKEN caches take q_len 1 only.
  * The workspace of pkv_decode_workspace_bytes serves any supported q_len.
  * Other arguments and guarantees as for pkv_paged_decode_attention. */
 PKV_API pkv_status pkv_paged_decode_attention_multi(

@@ -44,12 +44,13 @@ __all__ = [
     "pkv_decode_step_fused",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
-    "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "PKV_STEP_OVERLAP", "EXPORTED_SYMBOLS",
+    "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "PKV_FP8_E4M3_TOKEN", "PKV_STEP_OVERLAP",
+    "EXPORTED_SYMBOLS",
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE = 0, 1, 2, 3
 PKV_ERR_CUDA, PKV_ERR_BOUNDS, PKV_ERR_TIMEOUT = 4, 5, 6
-PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32 = 0, 1, 2, 3
+PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_F32, PKV_FP8_E4M3_TOKEN = 0, 1, 2, 3, 4
 PKV_STEP_OVERLAP = 1
 
 EXPORTED_SYMBOLS = (

@@ -64,8 +64,13 @@ pkv_status check_desc(const pkv_cache_desc* d) {
       if (d->head_dim != 64 && d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
       break;
     case PKV_FP8_E4M3:
+    case PKV_FP8_E4M3_TOKEN:
       if (d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-      if (d->k_scale == nullptr || d->v_scale == nullptr) return PKV_ERR_INVALID_ARG;
+      if (d->k_scale == nullptr) return PKV_ERR_INVALID_ARG;
+      if (d->cache_dtype == PKV_FP8_E4M3 && d->v_scale == nullptr) return PKV_ERR_INVALID_ARG;
+      // per token: one pool, a page's scales copied as one 128-byte line
+      if (d->cache_dtype == PKV_FP8_E4M3_TOKEN && !aligned(d->k_scale, 128))
+        return PKV_ERR_INVALID_ARG;
       break;
     default:
       return PKV_ERR_UNSUPPORTED;
@@ -76,8 +81,14 @@ pkv_status check_desc(const pkv_cache_desc* d) {
 }
 
 pkv::CacheKind kind_of(pkv_dtype t) {
-  return t == PKV_FP8_E4M3 ? pkv::kCacheE4M3 : (t == PKV_BF16 ? pkv::kCacheBF16 : pkv::kCacheF16);
+  switch (t) {
+    case PKV_FP8_E4M3: return pkv::kCacheE4M3;
+    case PKV_FP8_E4M3_TOKEN: return pkv::kCacheE4M3Tok;
+    case PKV_BF16: return pkv::kCacheBF16;
+    default: return pkv::kCacheF16;
+  }
 }
+bool is_fp8(pkv_dtype t) { return t == PKV_FP8_E4M3 || t == PKV_FP8_E4M3_TOKEN; }
 
 struct WsLayout {
   size_t ml_off, o_off, ticket_bytes, total;
@@ -145,7 +156,7 @@ namespace {
 pkv_status encode_cache_map(CUtensorMap* map, const void* cache, const pkv_cache_desc* d) {
   auto fn = encode_fn();
   if (fn == nullptr) return PKV_ERR_CUDA;
-  const bool fp8 = d->cache_dtype == PKV_FP8_E4M3;
+  const bool fp8 = is_fp8(d->cache_dtype);
   const cuuint64_t elem = fp8 ? 1 : 2;
   const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim,
                               (cuuint64_t)d->num_blocks * d->num_kv_heads * d->page_size};
@@ -164,7 +175,7 @@ pkv_status append_checks(const pkv_cache_desc* desc, const void* k_cache, const 
                          int32_t num_tokens, pkv_dtype kv_dtype) {
   if (!k_cache || !v_cache || !slot_mapping || !k || !v) return PKV_ERR_INVALID_ARG;
   if (kv_dtype != PKV_F16 && kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (desc->cache_dtype != PKV_FP8_E4M3 && kv_dtype != desc->cache_dtype)
+  if (!is_fp8(desc->cache_dtype) && kv_dtype != desc->cache_dtype)
     return PKV_ERR_INVALID_ARG;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(slot_mapping, 8))
@@ -189,7 +200,7 @@ pkv_status decode_checks(const pkv_cache_desc* desc, const void* q, const void* 
   if ((int64_t)batch * max_blocks_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
   if ((int64_t)max_blocks_per_seq * kPageSize >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (desc->cache_dtype != PKV_FP8_E4M3 && q_dtype != desc->cache_dtype)
+  if (!is_fp8(desc->cache_dtype) && q_dtype != desc->cache_dtype)
     return PKV_ERR_INVALID_ARG;
   if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
     return PKV_ERR_UNSUPPORTED;
@@ -274,13 +285,15 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
     switch (l.cache) {
       case pkv::kCacheF16: e = pkv::launch_decode_f16(l); break;
       case pkv::kCacheBF16: e = pkv::launch_decode_bf16(l); break;
-      default: e = pkv::launch_decode_e4m3(l); break;
+      case pkv::kCacheE4M3: e = pkv::launch_decode_e4m3(l); break;
+      default: e = pkv::launch_decode_e4m3_tok(l); break;
     }
   } else {
     switch (l.cache) {
       case pkv::kCacheF16: e = pkv::launch_decode_multi_f16(l); break;
       case pkv::kCacheBF16: e = pkv::launch_decode_multi_bf16(l); break;
-      default: e = pkv::launch_decode_multi_e4m3(l); break;
+      case pkv::kCacheE4M3: e = pkv::launch_decode_multi_e4m3(l); break;
+      default: e = cudaErrorNotSupported; break;  // per-token scales: one query token
     }
   }
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
@@ -307,6 +320,9 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
   a.block_tables = nullptr;
   a.context_lens = nullptr;
   a.MBS = 0;
+  a.scale_out = nullptr;
+  if (desc->cache_dtype == PKV_FP8_E4M3_TOKEN)  // the scale pool takes the rows' scales
+    a.scale_out = const_cast<float*>(desc->k_scale);
   a.k = k;
   a.v = v;
   a.k_scale = desc->k_scale;
@@ -339,7 +355,10 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* desc, void* k_cache, void* v_ca
   c.dst = dst_blocks;
   c.err_word = desc->err_word;
   c.block_bytes = (int64_t)desc->num_kv_heads * desc->page_size * desc->head_dim *
-                  (desc->cache_dtype == PKV_FP8_E4M3 ? 1 : 2);
+                  (is_fp8(desc->cache_dtype) ? 1 : 2);
+  c.scales = nullptr;  // per-token scales travel with their block
+  if (desc->cache_dtype == PKV_FP8_E4M3_TOKEN) c.scales = const_cast<float*>(desc->k_scale);
+  c.scales_per_block = desc->num_kv_heads * 2 * desc->page_size;
   c.NB = desc->num_blocks;
   const cudaError_t e = pkv::launch_copy_blocks(c, n, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -434,12 +453,12 @@ pkv_status pkv_decode_step_fused(const pkv_cache_desc* desc, const void* q, void
   if (st != PKV_OK || batch == 0) return st;
   if (!k || !v) return PKV_ERR_INVALID_ARG;
   if (kv_dtype != PKV_F16 && kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (desc->cache_dtype != PKV_FP8_E4M3 && kv_dtype != desc->cache_dtype)
+  if (!is_fp8(desc->cache_dtype) && kv_dtype != desc->cache_dtype)
     return PKV_ERR_INVALID_ARG;
   if (!aligned(k, 16) || !aligned(v, 16)) return PKV_ERR_INVALID_ARG;
   if ((flags & ~PKV_STEP_OVERLAP) != 0) return PKV_ERR_INVALID_ARG;
   const int overlap = (flags & PKV_STEP_OVERLAP) ? 1 : 0;
-  if (desc->cache_dtype == PKV_FP8_E4M3) {
+  if (is_fp8(desc->cache_dtype)) {
     // E4M3: the append kernel (each sequence's newest position, from its
     // table), then the attention overlapping its tail
     pkv::AppendParams a;
@@ -449,6 +468,8 @@ pkv_status pkv_decode_step_fused(const pkv_cache_desc* desc, const void* q, void
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.MBS = max_blocks_per_seq;
+    a.scale_out = nullptr;
+    if (desc->cache_dtype == PKV_FP8_E4M3_TOKEN) a.scale_out = const_cast<float*>(desc->k_scale);
     a.k = k;
     a.v = v;
     a.k_scale = desc->k_scale;
@@ -458,7 +479,7 @@ pkv_status pkv_decode_step_fused(const pkv_cache_desc* desc, const void* q, void
     a.Hkv = desc->num_kv_heads;
     a.d = desc->head_dim;
     a.NB = desc->num_blocks;
-    if (pkv::launch_append(a, pkv::kCacheE4M3, kv_dtype == PKV_BF16,
+    if (pkv::launch_append(a, kind_of(desc->cache_dtype), kv_dtype == PKV_BF16,
                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
       return PKV_ERR_CUDA;
     return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,

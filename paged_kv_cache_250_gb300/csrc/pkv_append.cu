@@ -14,6 +14,19 @@ namespace pkv {
 // skipped; slots past the pool are reported, never written.  For an E4M3
 // cache each value is divided by its head's scale (IEEE fp32) and encoded
 // round-to-nearest-even with saturation to +-448.
+// Largest magnitude of eight 16-bit values.
+template <bool IN_BF16>
+__device__ __forceinline__ float amax8(uint4 in) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = unpack2<IN_BF16>(w[i]);
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return m;
+}
+
 template <int CACHE, bool IN_BF16>
 __global__ void append_kernel(const AppendParams a) {
   // let a dependent decode kernel start its prologue while this one runs
@@ -45,12 +58,31 @@ __global__ void append_kernel(const AppendParams a) {
   const int64_t dst = ((blk * a.Hkv + h) * kPageSize + off) * per_row + part;
   const uint4 kin = reinterpret_cast<const uint4*>(a.k)[row * per_row + part];
   const uint4 vin = reinterpret_cast<const uint4*>(a.v)[row * per_row + part];
-  if constexpr (CACHE != kCacheE4M3) {
-    reinterpret_cast<uint4*>(a.k_cache)[dst] = kin;
-    reinterpret_cast<uint4*>(a.v_cache)[dst] = vin;
-  } else {
+  if constexpr (CACHE == kCacheE4M3) {
     reinterpret_cast<uint2*>(a.k_cache)[dst] = quantize8<IN_BF16>(kin, a.k_scale[h]);
     reinterpret_cast<uint2*>(a.v_cache)[dst] = quantize8<IN_BF16>(vin, a.v_scale[h]);
+  } else if constexpr (CACHE == kCacheE4M3Tok) {
+    // The row's own scale: its largest magnitude over 448 in IEEE fp32 (1 for
+    // an all-zero row).  A row is the 16 lanes of one half-warp (d = 128).
+    float ak = amax8<IN_BF16>(kin), av = amax8<IN_BF16>(vin);
+    const unsigned half = 0xffffu << (threadIdx.x & 16);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+      ak = fmaxf(ak, __shfl_xor_sync(half, ak, off));
+      av = fmaxf(av, __shfl_xor_sync(half, av, off));
+    }
+    const float ks = ak > 0.f ? __fdiv_rn(ak, 448.f) : 1.f;
+    const float vs = av > 0.f ? __fdiv_rn(av, 448.f) : 1.f;
+    reinterpret_cast<uint2*>(a.k_cache)[dst] = quantize8<IN_BF16>(kin, ks);
+    reinterpret_cast<uint2*>(a.v_cache)[dst] = quantize8<IN_BF16>(vin, vs);
+    if (part == 0) {  // pool [NB][Hkv][2][P]: the page's K scales, then its V scales
+      float* sp = a.scale_out + (blk * a.Hkv + h) * 2 * kPageSize + off;
+      sp[0] = ks;
+      sp[kPageSize] = vs;
+    }
+  } else {
+    reinterpret_cast<uint4*>(a.k_cache)[dst] = kin;
+    reinterpret_cast<uint4*>(a.v_cache)[dst] = vin;
   }
 }
 
@@ -66,6 +98,12 @@ cudaError_t launch_append(const AppendParams& a, CacheKind cache, bool in_bf16,
       append_kernel<kCacheE4M3, true><<<(unsigned)grid, block, 0, stream>>>(a);
     else
       append_kernel<kCacheE4M3, false><<<(unsigned)grid, block, 0, stream>>>(a);
+  } else if (cache == kCacheE4M3Tok) {
+    if (a.d != 128) return cudaErrorNotSupported;  // a row is one half-warp
+    if (in_bf16)
+      append_kernel<kCacheE4M3Tok, true><<<(unsigned)grid, block, 0, stream>>>(a);
+    else
+      append_kernel<kCacheE4M3Tok, false><<<(unsigned)grid, block, 0, stream>>>(a);
   } else {
     append_kernel<kCacheBF16, false><<<(unsigned)grid, block, 0, stream>>>(a);
   }

@@ -19,6 +19,11 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyParams c) {
   uint4* to = reinterpret_cast<uint4*>(base + (int64_t)dst * c.block_bytes);
   const int64_t n16 = c.block_bytes / 16;
   for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) __stcs(to + j, __ldcs(from + j));
+  if (c.scales != nullptr && blockIdx.y == 0) {
+    const int64_t n = c.scales_per_block;
+    for (int64_t j = threadIdx.x; j < n; j += blockDim.x)
+      c.scales[(int64_t)dst * n + j] = c.scales[(int64_t)src * n + j];
+  }
 }
 
 cudaError_t launch_copy_blocks(const CopyParams& c, int32_t n, cudaStream_t stream) {

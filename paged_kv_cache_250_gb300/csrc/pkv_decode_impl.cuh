@@ -81,12 +81,13 @@ struct Int {  // a compile-time count passed to a generic lambda
 
 template <int D, int CACHE>
 struct DecodeCfg {
-  static constexpr int kElem = CACHE == kCacheE4M3 ? 1 : 2;
+  static constexpr int kElem = cache_is_fp8((CacheKind)CACHE) ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;              // bytes per token row
   static constexpr int kBoxes = kRowBytes / 128;           // 128-byte TMA boxes per row
   static constexpr int kBoxBytes = kPageSize * 128;        // one box of a page
   static constexpr int kTileBytes = kPageSize * kRowBytes; // one K (or V) page
   static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kScaleBytes = decode_scale_bytes((CacheKind)CACHE);  // per stage
   static constexpr int kKSteps = D / 16;  // k-steps of the QK contraction
   static constexpr int kMTiles = D / 16;  // 16-row tiles of O^T
   static constexpr int kStages = decode_stages(D, (CacheKind)CACHE);
@@ -149,7 +150,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   constexpr int kGroup = kS >= 3 ? 2 : 1;
   // the one-kernel step writes new rows in the main loop for 16-bit caches
   // only (E4M3 steps enqueue the append kernel first)
-  constexpr bool kFusedAppend = QC == 1 && CACHE != kCacheE4M3;
+  constexpr bool kFp8 = cache_is_fp8((CacheKind)CACHE);
+  constexpr bool kTok = CACHE == kCacheE4M3Tok;  // one scale per token and KV head
+  constexpr bool kFusedAppend = QC == 1 && !kFp8;
 
   // the next kernel on the stream may launch (a programmatic dependent waits
   // for this one to complete before it reads what this one writes)
@@ -165,7 +168,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   const int lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
   const uint32_t ring = base + (uint32_t)(warp * kS * C::kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + (size_t)NW * kS * C::kStageBytes);
+  // per-token scales of the staged pages, beside the ring (E4M3 per token)
+  const uint32_t scl = base + (uint32_t)(NW * kS * C::kStageBytes + warp * kS * C::kScaleBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      base_ptr + (size_t)NW * kS * (C::kStageBytes + C::kScaleBytes));
   uint64_t* fbar = bars + NW * kS;  // [4] flush: full (even, odd), empty, padding
   // everything after the mbarriers stays 16-byte aligned (float4 in mbuf)
   static_assert((NW * kS * 8) % 16 == 0 && (NW * kDescRing * 8) % 16 == 0, "smem alignment");
@@ -410,11 +416,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const uint32_t kt = ring + (uint32_t)(slot * C::kStageBytes);
       const uint32_t vt = kt + C::kTileBytes;
       if (dsc.x >= 0) {
-        mbar_arrive_expect_tx(bar, C::kStageBytes);
+        mbar_arrive_expect_tx(bar, C::kStageBytes + C::kScaleBytes);
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx) {
           tma_load_2d(kt + bx * C::kBoxBytes, &tmk, bar, bx * (128 / C::kElem), dsc.x, pol);
           tma_load_2d(vt + bx * C::kBoxBytes, &tmv, bar, bx * (128 / C::kElem), dsc.x, pol);
+        }
+        if constexpr (kTok) {  // the page's 16 K scales, then its 16 V scales: one line
+          bulk_load(scl + (uint32_t)(slot * C::kScaleBytes), p.k_scale + 2 * dsc.x,
+                    C::kScaleBytes, bar, pol);
         }
       } else {
         mbar_arrive(bar);  // nothing to load; complete the phase
@@ -445,7 +455,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 
   // d of O^T rows r8 and r8 + 8 in m-tile mt
   auto d_of = [&](int mt, int half) -> int {
-    if constexpr (CACHE != kCacheE4M3) return 16 * mt + r8 + 8 * half;
+    if constexpr (!kFp8) return 16 * mt + r8 + 8 * half;
     else return 32 * (mt >> 1) + 2 * r8 + (mt & 1) + 16 * half;
   };
 
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const bool real = col_real(col);
     const uint16_t* qrow =
         reinterpret_cast<const uint16_t*>(p.q) + (real ? col_row(b, h, col) : 0) * D;
-    if constexpr (CACHE != kCacheE4M3) {
+    if constexpr (!kFp8) {
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
         uint32_t b0 = 0, b1 = 0;
@@ -510,7 +520,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 4; ++e) s[e] = 0.f;
-    if constexpr (CACHE != kCacheE4M3) {
+    if constexpr (!kFp8) {
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
         uint32_t a[4];
@@ -550,7 +560,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
       mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
     }
-    if constexpr (CACHE != kCacheE4M3) {
+    if constexpr (!kFp8) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         uint32_t a[4];
@@ -595,6 +605,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   auto compute_pages = [&](auto npc, const uint32_t* kt, const int* valids) {
     constexpr int NP = decltype(npc)::value;
     float x[NP][4];
+    float ksc[NP][2], vsc[NP][2];  // per-token K and V scales of rows r8, r8 + 8
+    if constexpr (kTok) {  // read first: their latency hides under the QK MMAs
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const uint32_t sp = scl + ((kt[i] - ring) / C::kStageBytes) * C::kScaleBytes;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ksc[i][0]) : "r"(sp + r8 * 4));
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ksc[i][1]) : "r"(sp + (r8 + 8) * 4));
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vsc[i][0]) : "r"(sp + (kPageSize + r8) * 4));
+        asm volatile("ld.shared.f32 %0, [%1];"
+                     : "=f"(vsc[i][1]) : "r"(sp + (kPageSize + r8 + 8) * 4));
+      }
+    }
 #pragma unroll
     for (int i = 0; i < NP; ++i) qk_page(kt[i], x[i]);
     float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -604,6 +626,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const int rem = v & kRemMask;  // tokens from the page's start to the context's end
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[i][e] *= c2;
+      if constexpr (kTok) {
+        x[i][0] *= ksc[i][0];  // rows past the context are masked below
+        x[i][1] *= ksc[i][0];
+        x[i][2] *= ksc[i][1];
+        x[i][3] *= ksc[i][1];
+        if (r8 >= rem) vsc[i][0] = 0.f;  // their P is 0; their scale may be anything
+        if (r8 + 8 >= rem) vsc[i][1] = 0.f;
+      }
       if constexpr (QC == 1) {
         if (rem < kPageSize) {
           if (r8 >= rem) x[i][0] = x[i][1] = -INFINITY;
@@ -672,10 +702,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const float p0 = exp2f(x[i][0] - mu0), p1 = exp2f(x[i][1] - mu1);
-      const float p2 = exp2f(x[i][2] - mu0), p3 = exp2f(x[i][3] - mu1);
+      float p0 = exp2f(x[i][0] - mu0), p1 = exp2f(x[i][1] - mu1);
+      float p2 = exp2f(x[i][2] - mu0), p3 = exp2f(x[i][3] - mu1);
       l2[0] += p0 + p2;
       l2[1] += p1 + p3;
+      if constexpr (kTok) {  // P.V weights carry each token's V scale
+        p0 *= vsc[i][0];
+        p1 *= vsc[i][0];
+        p2 *= vsc[i][1];
+        p3 *= vsc[i][1];
+      }
       // P as hi + lo 16-bit parts, transposed into B fragments
       const uint32_t h01 = pack2<kBF>(p0, p1), h23 = pack2<kBF>(p2, p3);
       const float2 f01 = unpack2<kBF>(h01), f23 = unpack2<kBF>(h23);
@@ -1155,7 +1191,7 @@ cudaError_t dispatch_split(const DecodeLaunch& l) {
   const int g = l.group;
 #define PKV_CASE(DD, GG) \
   if (d == DD && g == GG) return launch_split<DD, GG, 1, CACHE, QBF16>(l);
-  if constexpr (CACHE != kCacheE4M3) {
+  if constexpr (!cache_is_fp8((CacheKind)CACHE)) {
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   }
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
@@ -1171,7 +1207,7 @@ cudaError_t dispatch_split_multi(const DecodeLaunch& l) {
   const int qc = l.qcap;
 #define PKV_CASE(DD, GG, QQ) \
   if (d == DD && g == GG && qc == QQ) return launch_split<DD, GG, QQ, CACHE, QBF16>(l);
-  if constexpr (CACHE != kCacheE4M3) {
+  if constexpr (!cache_is_fp8((CacheKind)CACHE)) {
     PKV_CASE(64, 1, 2) PKV_CASE(64, 1, 4) PKV_CASE(64, 1, 8)
     PKV_CASE(64, 2, 2) PKV_CASE(64, 2, 4) PKV_CASE(64, 4, 2)
   }

@@ -14,7 +14,11 @@ constexpr int kPageSize = 16;  // tokens per block: the only page size built
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeCtasPerSm = 2;
 
-enum CacheKind { kCacheF16 = 0, kCacheBF16 = 1, kCacheE4M3 = 2 };
+// E4M3: one fp32 scale per KV head; E4M3 per token: one K and one V scale per
+// (block, KV head, slot), in one pool [NB][Hkv][2][P] (a page's 16 K scales,
+// then its 16 V scales: one 128-byte line).
+enum CacheKind { kCacheF16 = 0, kCacheBF16 = 1, kCacheE4M3 = 2, kCacheE4M3Tok = 3 };
+__host__ __device__ constexpr bool cache_is_fp8(CacheKind c) { return c == kCacheE4M3 || c == kCacheE4M3Tok; }
 
 // A CTA's share holds at least about kRangeMin cost units (fewer CTAs run
 // when the batch is small: a short context is not worth splitting) and is
@@ -28,7 +32,11 @@ constexpr int kSegCost = 9;
 // Shared-memory plan of the decode kernel (host and device agree on it).
 constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
 constexpr int decode_stage_bytes(int d, CacheKind c) {
-  return 2 * kPageSize * d * (c == kCacheE4M3 ? 1 : 2);
+  return 2 * kPageSize * d * (cache_is_fp8(c) ? 1 : 2);
+}
+// per-token scales of one staged page (K then V), kept beside the page ring
+constexpr int decode_scale_bytes(CacheKind c) {
+  return c == kCacheE4M3Tok ? 2 * kPageSize * 4 : 0;
 }
 // alignment slack + descriptor rings + merge buffers + merge flags +
 // mbarriers (8 stages max per warp, 4 slots for the flush hand-off)
@@ -43,7 +51,7 @@ constexpr int kDecodeSmemTarget = 113 * 1024;
 constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
 constexpr int decode_stages(int d, CacheKind c) {
   return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d) - 2600) /
-                             (kDecodeWarps * decode_stage_bytes(d, c)));
+                             (kDecodeWarps * (decode_stage_bytes(d, c) + decode_scale_bytes(c))));
 }
 
 // Arguments of the decode kernel (one CTA = one contiguous share of all
@@ -93,6 +101,8 @@ struct AppendParams {
   const int32_t* block_tables;   // of sequence t, through its block table
   const int32_t* context_lens;
   int32_t MBS;
+  float* scale_out;              // E4M3 per token: the scale pool [NB][Hkv][2][P] the
+                                 // rows' scales go to (NULL otherwise)
   const void* k;
   const void* v;
   const float* k_scale;
@@ -104,7 +114,8 @@ struct AppendParams {
 // Dynamic shared memory the split kernel needs for a batch of B sequences.
 inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
   return (size_t)decode_fixed_smem(d) +
-         (size_t)kDecodeWarps * decode_stages(d, cache) * decode_stage_bytes(d, cache) +
+         (size_t)kDecodeWarps * decode_stages(d, cache) *
+             (decode_stage_bytes(d, cache) + decode_scale_bytes(cache)) +
          (size_t)(5 * B + 2) * 4;
 }
 
@@ -113,6 +124,7 @@ inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
 cudaError_t launch_decode_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_e4m3(const DecodeLaunch& l);
+cudaError_t launch_decode_e4m3_tok(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_e4m3(const DecodeLaunch& l);
@@ -133,6 +145,8 @@ struct CopyParams {
   int32_t* err_word;
   int64_t block_bytes;  // one block of one cache: Hkv * P * d * element bytes
   int32_t NB;
+  float* scales;        // E4M3 per token: the scale pool, copied with its block
+  int32_t scales_per_block;  // Hkv * 2 * P
 };
 
 cudaError_t launch_copy_blocks(const CopyParams& c, int32_t n, cudaStream_t stream);

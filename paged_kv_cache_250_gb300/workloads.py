@@ -20,7 +20,10 @@ Recipe (per workload):
     code 0x7F), so a read outside the context shows up in the output;
   * FP8 cache: one fp32 scale per KV head for K and one for V, amax/448 over
     that head's drawn values; stored bytes are torch's float8_e4m3fn cast of
-    value / scale (a library routine, used here only to draw input bytes).
+    value / scale (a library routine, used here only to draw input bytes);
+  * FP8 cache with per-token scales ("e4m3tok"): the same, with one scale per
+    (token, KV head) row, amax/448 over the row, held in one scale pool
+    [NB][Hkv][2][P] (K scales, then V scales; NaN in unused slots).
 """
 from __future__ import annotations
 
@@ -42,7 +45,7 @@ class DecodeConfig:
     q_heads: int
     kv_heads: int
     head_dim: int
-    cache: str                       # "f16" | "bf16" | "e4m3"
+    cache: str                       # "f16" | "bf16" | "e4m3" | "e4m3tok"
     ctx: Union[int, Tuple[int, int]]  # fixed length or (lo, hi) uniform
     table: str = "permuted"          # "permuted" | "identity"
     seed: int = 0
@@ -61,12 +64,16 @@ class DecodeConfig:
 
     @property
     def qdt(self) -> torch.dtype:
-        name = self.q_dtype or ("bf16" if self.cache == "e4m3" else self.cache)
+        name = self.q_dtype or ("bf16" if self.is_fp8 else self.cache)
         return {"f16": torch.float16, "bf16": torch.bfloat16}[name]
 
     @property
+    def is_fp8(self) -> bool:
+        return self.cache in ("e4m3", "e4m3tok")
+
+    @property
     def cache_elem_bytes(self) -> int:
-        return 1 if self.cache == "e4m3" else 2
+        return 1 if self.is_fp8 else 2
 
 
 CONFIGS = {
@@ -88,6 +95,10 @@ CONFIGS = {
                      spare_blocks=64,
                      description="8B shape, batch 64, context 8192, E4M3 cache with per-head "
                                  "fp32 scales, bf16 q and output"),
+        DecodeConfig("fp8tok_8b_b64_ctx8192_e4m3", 64, 32, 8, 128, "e4m3tok", 8192, seed=3,
+                     spare_blocks=64,
+                     description="8B shape, batch 64, context 8192, E4M3 cache with one fp32 "
+                                 "scale per token and KV head, bf16 q and output"),
         DecodeConfig("mha_7b_b64_ctx8192_bf16", 64, 32, 32, 128, "bf16", 8192, seed=3,
                      spare_blocks=64,
                      description="7B MHA shape, 32/32 heads, batch 64, context 8192, bf16"),
@@ -124,7 +135,7 @@ class DecodeWorkload:
     V_stored: torch.Tensor
     k_cache: torch.Tensor        # [NB][Hkv][P][d] stored dtype (uint8 for e4m3)
     v_cache: torch.Tensor
-    k_scale: Optional[torch.Tensor] = None  # fp32 [Hkv] (e4m3 only)
+    k_scale: Optional[torch.Tensor] = None  # fp32 [Hkv] (e4m3); [NB][Hkv][2][P] (e4m3tok)
     v_scale: Optional[torch.Tensor] = None
     extra: dict = field(default_factory=dict)
 
@@ -140,7 +151,8 @@ class DecodeWorkload:
 
 
 def _store_dtype(cache: str) -> torch.dtype:
-    return {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8}[cache]
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8,
+            "e4m3tok": torch.uint8}[cache]
 
 
 def draw_context_lengths(cfg: DecodeConfig, gen: torch.Generator) -> torch.Tensor:
@@ -178,7 +190,7 @@ def generate(cfg: DecodeConfig, device: Union[str, torch.device] = "cpu",
     B, Hq, Hkv, d = cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim
     T = max(1, int(ctx.max()))
     g_dev = torch.Generator(device=device).manual_seed(cfg.seed + 1000)
-    in_dt = cfg.qdt if cfg.cache != "e4m3" else torch.bfloat16
+    in_dt = cfg.qdt if not cfg.is_fp8 else torch.bfloat16
     q = torch.randn(B, Hq, d, generator=g_dev, device=device).to(cfg.qdt)
     K_log = torch.randn(B, T, Hkv, d, generator=g_dev, device=device).to(in_dt)
     V_log = torch.randn(B, T, Hkv, d, generator=g_dev, device=device).to(in_dt)
@@ -193,7 +205,22 @@ def generate(cfg: DecodeConfig, device: Union[str, torch.device] = "cpu",
     slot = torch.where(ctx_d > 0, slot, torch.full_like(slot, -1))
 
     k_scale = v_scale = None
-    if cfg.cache == "e4m3":
+    extra = {}
+    if cfg.cache == "e4m3tok":
+        ks_tok = K_log.float().abs().amax(dim=3) / E4M3_MAX  # [B][T][Hkv]
+        vs_tok = V_log.float().abs().amax(dim=3) / E4M3_MAX
+        ks_tok = torch.where(ks_tok > 0, ks_tok, torch.ones_like(ks_tok))
+        vs_tok = torch.where(vs_tok > 0, vs_tok, torch.ones_like(vs_tok))
+        K_st = (K_log.float() / ks_tok[..., None]).clamp(-E4M3_MAX, E4M3_MAX)
+        V_st = (V_log.float() / vs_tok[..., None]).clamp(-E4M3_MAX, E4M3_MAX)
+        K_stored = K_st.to(torch.float8_e4m3fn).view(torch.uint8)
+        V_stored = V_st.to(torch.float8_e4m3fn).view(torch.uint8)
+        del K_st, V_st
+        poison = E4M3_NAN
+        extra = {"k_tok_scale": ks_tok, "v_tok_scale": vs_tok}
+        k_scale = torch.full((NB, Hkv, 2, PAGE), float("nan"), dtype=torch.float32,
+                             device=device)
+    elif cfg.cache == "e4m3":
         k_scale = (K_log.float().abs().amax(dim=(0, 1, 3)) / E4M3_MAX).clamp(min=1e-12)
         v_scale = (V_log.float().abs().amax(dim=(0, 1, 3)) / E4M3_MAX).clamp(min=1e-12)
         K_st = (K_log.float() / k_scale[None, None, :, None]).clamp(-E4M3_MAX, E4M3_MAX)
@@ -222,10 +249,14 @@ def generate(cfg: DecodeConfig, device: Union[str, torch.device] = "cpu",
         off = ti_t % PAGE
         k_cache[blk, :, off, :] = K_stored[bi_t, ti_t]
         v_cache[blk, :, off, :] = V_stored[bi_t, ti_t]
+        if cfg.cache == "e4m3tok":
+            k_scale[blk, :, 0, off] = extra["k_tok_scale"][bi_t, ti_t]
+            k_scale[blk, :, 1, off] = extra["v_tok_scale"][bi_t, ti_t]
     return DecodeWorkload(cfg=cfg, ctx=ctx, block_tables=tables, slot_mapping=slot.cpu(),
                           num_blocks=NB, q=q, k_new=k_new, v_new=v_new, K_log=K_log,
                           V_log=V_log, K_stored=K_stored, V_stored=V_stored,
-                          k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale)
+                          k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                          extra=extra)
 
 
 def cache_bytes_per_step(cfg: DecodeConfig, ctx: torch.Tensor) -> int:

@@ -21,11 +21,12 @@ TOL_16BIT = 2e-3   # max abs error vs the oracle, bf16/fp16 cache, fp32 accumula
 TOL_FP8 = 3e-2     # max abs error vs the oracle on the dequantised cache
 
 _DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-_CODE = {"f16": pkv.PKV_F16, "bf16": pkv.PKV_BF16, "e4m3": pkv.PKV_FP8_E4M3}
+_CODE = {"f16": pkv.PKV_F16, "bf16": pkv.PKV_BF16, "e4m3": pkv.PKV_FP8_E4M3,
+         "e4m3tok": pkv.PKV_FP8_E4M3_TOKEN}
 
 
 def tolerance(cfg) -> float:
-    return TOL_FP8 if cfg.cache == "e4m3" else TOL_16BIT
+    return TOL_FP8 if cfg.is_fp8 else TOL_16BIT
 
 
 def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
@@ -44,10 +45,23 @@ def logical_kv_fp64(w: wl.DecodeWorkload, b: int, h: int) -> Tuple[np.ndarray, n
     codes (prefix) or the oracle's own encoding of the new token, decoded and
     scaled by the oracle's codec."""
     n = int(w.ctx[b])
-    if w.cfg.cache != "e4m3":
+    if not w.cfg.is_fp8:
         K = w.K_log[b, :n, h].double().cpu().numpy()
         V = w.V_log[b, :n, h].double().cpu().numpy()
         return K, V
+    if w.cfg.cache == "e4m3tok":  # one scale per row; the new row's by the oracle
+        Kc = w.K_stored[b, :n, h].cpu().numpy().copy()
+        Vc = w.V_stored[b, :n, h].cpu().numpy().copy()
+        ks = w.extra["k_tok_scale"][b, :n, h].float().cpu().numpy().copy()
+        vs = w.extra["v_tok_scale"][b, :n, h].float().cpu().numpy().copy()
+        if n > 0:
+            kn = w.k_new[b, h].float().cpu().numpy()
+            vn = w.v_new[b, h].float().cpu().numpy()
+            ks[n - 1] = oracle.e4m3_token_scale(kn)
+            vs[n - 1] = oracle.e4m3_token_scale(vn)
+            Kc[n - 1] = oracle.e4m3_quantize(kn, ks[n - 1])
+            Vc[n - 1] = oracle.e4m3_quantize(vn, vs[n - 1])
+        return oracle.e4m3_dequantize_rows(Kc, ks), oracle.e4m3_dequantize_rows(Vc, vs)
     ks = float(w.k_scale[h])
     vs = float(w.v_scale[h])
     Kc = w.K_stored[b, :n, h].cpu().numpy().copy()
