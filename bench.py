@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -82,6 +83,16 @@ def measured_peak():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return PEAK_FALLBACK_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor peak: the burst figure (a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -631,6 +642,81 @@ def run_multi_query(args, cfg, device, windowed: bool = False):
             "gpu_launches": K}
 
 
+def prefill_flops(ctx: torch.Tensor, chunk: int, q_heads: int, d: int) -> int:
+    """Causal attention FLOPs of the prefill: the row at position p scores and
+    weighs p + 1 positions, 4 d flops each (q.k and p.v), per query head."""
+    total = 0
+    for n in ctx.tolist():
+        c = min(chunk, n)
+        total += c * n - c * (c - 1) // 2  # sum of (p + 1) over the chunk's rows
+    return 4 * d * q_heads * total
+
+
+def run_prefill(args, cfg, device):
+    """pkv_paged_prefill_attention alone: every sequence's last `chunk`
+    positions (already in the cache) attend causally over its whole context.
+    K calls in one CUDA graph, CUDA events around it; causal FLOPs (QK and PV)
+    over the time, against the measured bf16 tensor peak."""
+    st = Step(cfg, device, 1, 0)
+    st.append(0, torch.cuda.current_stream(device))  # the newest position too
+    torch.cuda.synchronize(device)
+    chunks = [min(args.chunk, int(n)) for n in st.w.ctx.tolist()]
+    starts = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32,
+                          device=device)
+    total = int(starts[-1])
+    g = torch.Generator().manual_seed(cfg.seed + 91)
+    q = torch.randn(total, cfg.q_heads, cfg.head_dim, generator=g).to(cfg.qdt).to(device)
+    out = torch.empty(total, cfg.q_heads, cfg.head_dim, dtype=st.out.dtype, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def call():
+        pkv.pkv_paged_prefill_attention(st.desc, q, st.kc[0], st.vc[0], st.tables, st.ctx,
+                                        starts, max(chunks), cfg.softmax_scale, out,
+                                        stream=stream)
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        call()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(K):
+            call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.2)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    if int(st.err.item()) != 0:
+        raise RuntimeError("device error word set")
+    ms = e0.elapsed_time(e1) / K
+    flops = prefill_flops(st.w.ctx, args.chunk, cfg.q_heads, cfg.head_dim)
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = measured_tensor_peak()
+    return {"metric": "paged prefill attention TFLOP/s (causal QK and PV flops)",
+            "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K,
+            "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "f16": "f16"}[cfg.cache],
+            "data": "synthetic (seeded N(0,1) q/k/v, the workload's lengths and tables)",
+            "config": {**workload_config(cfg, st.w.ctx), "chunk": args.chunk,
+                       "query_rows": total, "flops_per_call": flops,
+                       "timing": "K calls in one CUDA graph, CUDA events on the stream"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak[0],
+                         "unit": "TFLOP/s", "frac": round(tflops / peak[0], 4),
+                         "traffic": None, "kernel": "prefill_kernel (tcgen05)",
+                         "peak_kind": peak[1]},
+            "gpu_launches": K, "clocks": sampler.summary(t0, t1)}
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -641,9 +727,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="decode_step",
-                    choices=["decode_step", "copy_blocks", "multi_query", "window"],
-                    help="decode_step (the default line), copy_blocks, multi_query or window "
-                         "alone")
+                    choices=["decode_step", "copy_blocks", "multi_query", "window", "prefill"],
+                    help="decode_step (the default line), copy_blocks, multi_query, window or "
+                         "prefill alone")
+    ap.add_argument("--chunk", type=int, default=2048,
+                    help="prefill rows per sequence (its last positions)")
     ap.add_argument("--qlen", type=int, default=2,
                     help="query tokens per sequence (multi_query, window)")
     ap.add_argument("--window", type=int, default=4096, help="window length (window)")
@@ -669,6 +757,10 @@ def main():
     if args.op == "copy_blocks":
         if rank == 0:
             print(json.dumps(run_copy_blocks(args, device)), flush=True)
+        return
+    if args.op == "prefill":
+        if rank == 0:
+            print(json.dumps(run_prefill(args, cfg, device)), flush=True)
         return
     if args.op in ("multi_query", "window"):
         if rank == 0:

@@ -241,6 +241,36 @@ PKV_API pkv_status pkv_decode_step(
     void* out, pkv_dtype q_dtype, pkv_dtype out_dtype, void* workspace,
     size_t workspace_bytes, pkv_stream_t stream);
 
+/* Paged prefill attention: a chunk of new tokens per sequence, whose K and V
+ * are already in the cache, attends causally over the sequence's whole
+ * context through its block table ([KVFA] opening section: the prefill phase
+ * processes the prompt in one parallel pass; continuous-batching section:
+ * chunked prefill reads each sequence's pages through its table).  Row j of
+ * sequence b's chunk sits at position context_lens[b] - n_b + j (n_b its
+ * row count) and attends to positions 0 .. that position.  Runs on the
+ * tensor cores (tcgen05, accumulators in tensor memory); 16-bit caches with
+ * head_dim 128 (others return PKV_ERR_UNSUPPORTED).
+ *   q             [total_q][num_q_heads][128] of q_dtype (= cache_dtype);
+ *                 sequence b's rows are q_start[b] .. q_start[b + 1] - 1.
+ *   q_start       int32 [batch + 1], device, non-decreasing, q_start[batch]
+ *                 <= total_q.
+ *   max_q_len     host: an upper bound on q_start[b + 1] - q_start[b]; it
+ *                 sizes the launch.
+ *   context_lens  tokens of each sequence, the chunk included (>= n_b).
+ *   out           [total_q][num_q_heads][128] of out_dtype (F16 | BF16 | F32).
+ * A sequence whose rows, length or table break these rules is a device-
+ * detected PKV_ERR_BOUNDS; its output rows are then not written.  No
+ * workspace.  Inputs are read after the preceding kernel on the stream
+ * completes (the kernel is launched as a programmatic dependent).  Results
+ * are deterministic: each output row is one CTA's fixed sequence of MMAs. */
+PKV_API pkv_status pkv_paged_prefill_attention(
+    const pkv_cache_desc* desc, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* q_start, int32_t batch,
+    int32_t total_q, int32_t max_q_len, int32_t max_blocks_per_seq,
+    float scale, void* out, pkv_dtype q_dtype, pkv_dtype out_dtype,
+    pkv_stream_t stream);
+
 /* One decode step in ONE kernel: pkv_decode_step with each sequence's new
  * token placed at its position context_lens[b] - 1, i.e. in block
  * block_tables[b][(context_lens[b] - 1) / P] at offset (context_lens[b] - 1)

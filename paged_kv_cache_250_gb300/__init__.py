@@ -10,6 +10,8 @@ memory and streams.  The functions carry the C names:
     pkv_paged_decode_attention_multi  q_len new tokens per sequence, causal
     pkv_paged_decode_attention_window  the same under a sliding window with
                                   attention sinks
+    pkv_paged_prefill_attention   a chunk of new tokens per sequence, causal,
+                                  on the tensor cores (tcgen05)
     pkv_decode_step               both, validated together, the attention
                                   kernel overlapping the append's tail
     pkv_decode_step_fused         both in one kernel (new token at its
@@ -41,7 +43,7 @@ __all__ = [
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES", "pkv_copy_blocks",
     "pkv_paged_decode_attention_multi", "pkv_paged_decode_attention_window",
-    "pkv_decode_step_fused",
+    "pkv_decode_step_fused", "pkv_paged_prefill_attention",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
     "PKV_ERR_CUDA", "PKV_ERR_BOUNDS", "PKV_ERR_TIMEOUT",
     "PKV_F16", "PKV_BF16", "PKV_FP8_E4M3", "PKV_F32", "PKV_FP8_E4M3_TOKEN", "PKV_STEP_OVERLAP",
@@ -57,7 +59,7 @@ EXPORTED_SYMBOLS = (
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "pkv_copy_blocks", "pkv_paged_decode_attention_multi",
-    "pkv_paged_decode_attention_window", "pkv_decode_step_fused",
+    "pkv_paged_decode_attention_window", "pkv_decode_step_fused", "pkv_paged_prefill_attention",
 )
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -123,6 +125,9 @@ def load_library():
         lib.pkv_paged_decode_attention_multi.restype = I32
         lib.pkv_paged_decode_attention_multi.argtypes = [D, P, P, P, P, P, I32, I32, I32, I32,
                                                          ctypes.c_float, P, I32, I32, P, SZ, P]
+        lib.pkv_paged_prefill_attention.restype = I32
+        lib.pkv_paged_prefill_attention.argtypes = [D, P, P, P, P, P, P, I32, I32, I32, I32,
+                                                    ctypes.c_float, P, I32, I32, P]
         lib.pkv_decode_step_fused.restype = I32
         lib.pkv_decode_step_fused.argtypes = [D, P, P, P, P, P, I32, P, P, I32, I32, I32,
                                               ctypes.c_float, P, I32, I32, P, SZ, I32, P]
@@ -319,6 +324,33 @@ def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _stream_handle(stream, q.device))
     _check(st, "pkv_decode_step")
+
+
+def pkv_paged_prefill_attention(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                context_lens: torch.Tensor, q_start: torch.Tensor,
+                                max_q_len: int, scale: float, out: torch.Tensor,
+                                stream=None) -> None:
+    """q/out: [total_q][Hq][128]; sequence b's rows q_start[b] .. q_start[b+1]-1
+    are its last positions, causal; q_start int32 [B+1] on the device."""
+    lib = load_library()
+    for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (q_start, "q_start")):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must be [total_q][Hq][d]")
+    B, mbs = int(block_tables.shape[0]), int(block_tables.shape[1])
+    if q_start.numel() != B + 1:
+        raise ValueError("q_start needs batch + 1 entries")
+    st = lib.pkv_paged_prefill_attention(
+        ctypes.byref(desc), _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(context_lens, "context_lens"), _dev_ptr(q_start, "q_start"), B,
+        int(q.shape[0]), int(max_q_len), mbs, float(scale), _dev_ptr(out, "out"),
+        _DTYPE_CODE.get(q.dtype, -1), _DTYPE_CODE.get(out.dtype, -1),
+        _stream_handle(stream, q.device))
+    _check(st, "pkv_paged_prefill_attention")
 
 
 def pkv_decode_step_fused(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,

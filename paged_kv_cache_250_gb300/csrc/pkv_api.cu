@@ -439,6 +439,68 @@ pkv_status pkv_decode_step(const pkv_cache_desc* desc, const void* q, void* k_ca
                      workspace, workspace_bytes, stream, /*early_prologue=*/1);
 }
 
+pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* q_start,
+                                       int32_t batch, int32_t total_q, int32_t max_q_len,
+                                       int32_t max_blocks_per_seq, float scale, void* out,
+                                       pkv_dtype q_dtype, pkv_dtype out_dtype,
+                                       pkv_stream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || total_q < 0 || max_q_len < 0 || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !q_start || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (desc->cache_dtype != PKV_F16 && desc->cache_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (q_dtype != desc->cache_dtype) return PKV_ERR_INVALID_ARG;
+  if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+    return PKV_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if ((int64_t)batch * max_blocks_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * kPageSize >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)total_q * desc->num_q_heads >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(q_start, 4))
+    return PKV_ERR_INVALID_ARG;
+  pkv::PrefillLaunch l;
+  st = encode_cache_map(&l.tmap_k, k_cache, desc);
+  if (st != PKV_OK) return st;
+  st = encode_cache_map(&l.tmap_v, v_cache, desc);
+  if (st != PKV_OK) return st;
+  auto fn = encode_fn();
+  if (fn == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)desc->num_q_heads, (cuuint64_t)total_q};
+  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)desc->num_q_heads * 128 * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&l.tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PKV_ERR_CUDA;
+  l.p.q_start = q_start;
+  l.p.context_lens = context_lens;
+  l.p.block_tables = block_tables;
+  l.p.out = out;
+  l.p.err_word = desc->err_word;
+  l.p.B = batch;
+  l.p.Hq = desc->num_q_heads;
+  l.p.Hkv = desc->num_kv_heads;
+  l.p.NB = desc->num_blocks;
+  l.p.MBS = max_blocks_per_seq;
+  l.p.total_q = total_q;
+  l.p.tiles_per_seq = (max_q_len + 127) / 128;
+  l.p.out_dtype = out_dtype;
+  l.p.scale_log2 = scale * 1.4426950408889634f;
+  l.bf16 = desc->cache_dtype == PKV_BF16;
+  l.stream = reinterpret_cast<cudaStream_t>(stream);
+  if ((int64_t)batch * l.p.tiles_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+  return pkv::launch_prefill(l) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_decode_step_fused(const pkv_cache_desc* desc, const void* q, void* k_cache,
                                  void* v_cache, const void* k, const void* v,
                                  pkv_dtype kv_dtype, const int32_t* block_tables,

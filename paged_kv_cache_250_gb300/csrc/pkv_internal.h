@@ -151,4 +151,27 @@ struct CopyParams {
 
 cudaError_t launch_copy_blocks(const CopyParams& c, int32_t n, cudaStream_t stream);
 
+// Paged prefill (pkv_prefill.cu): one CTA per 128 query rows of one
+// (sequence, query head).
+struct PrefillParams {
+  const int32_t* q_start;       // [B+1] first query row of each sequence
+  const int32_t* context_lens;  // [B]
+  const int32_t* block_tables;  // [B][MBS]
+  void* out;                    // [total_q][Hq][128]
+  int32_t* err_word;
+  int32_t B, Hq, Hkv, NB, MBS, total_q, tiles_per_seq;
+  pkv_dtype out_dtype;
+  float scale_log2;
+};
+struct PrefillLaunch {
+  PrefillParams p;
+  CUtensorMap tmap_q;  // [total_q][Hq][128], boxes of 128 rows x 64 columns
+  CUtensorMap tmap_k;  // the cache maps of the decode kernel
+  CUtensorMap tmap_v;
+  bool bf16;
+  cudaStream_t stream;
+};
+size_t prefill_smem_bytes();
+cudaError_t launch_prefill(const PrefillLaunch& l);
+
 }  // namespace pkv

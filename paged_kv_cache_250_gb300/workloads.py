@@ -87,6 +87,11 @@ CONFIGS = {
                      seed=1, spare_blocks=64,
                      description="Llama-3-8B-shaped layer: batch 32, 32/8 heads, d 128, bf16, "
                                  "context uniform in [1, 4096], permuted shared pool"),
+        DecodeConfig("llama3_8b_b8_ctx8192_bf16", 8, 32, 8, 128, "bf16", 8192, seed=5,
+                     spare_blocks=64,
+                     description="Llama-3-8B-shaped layer, 8 sequences of 8192 tokens (the "
+                                 "prefill workload: each sequence's last 2048 positions are "
+                                 "its new chunk)"),
         DecodeConfig("llama3_70b_b8_ctx32768_bf16", 8, 64, 8, 128, "bf16", 32768, seed=2,
                      spare_blocks=64,
                      description="Llama-3-70B-shaped layer: batch 8, 64/8 heads, d 128, bf16, "

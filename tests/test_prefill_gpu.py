@@ -1,0 +1,133 @@
+"""Paged prefill attention on the tensor cores (tcgen05) through the C ABI,
+against the oracle's causal multi-query attention (each new row at position
+ctx - n + j sees positions 0 .. itself).
+
+"KV Cache & Flash Attention." (kvcache-7e2.pages.dev): the prefill phase
+processes the prompt in one parallel pass; continuous-batching section:
+chunked prefill reads each sequence's pages through its table."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_250_gb300 as pkv
+from paged_kv_cache_250_gb300 import workloads as wl
+from harness import GpuRun, logical_kv_fp64, assert_close
+
+pytestmark = pytest.mark.gpu
+
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def _setup(name, Hq, Hkv, cache, ctx, seed):
+    cfg = wl.small_config(name, len(ctx), Hq, Hkv, 128, cache, 1, seed=seed)
+    w = wl.generate(cfg, ctx_override=torch.tensor(ctx))
+    run = GpuRun(w)
+    run.append()  # every position of every sequence is now in the cache
+    return cfg, w, run
+
+
+def _prefill(run, cfg, chunks, out_dtype="f32", seed=0, max_q_len=None):
+    g = torch.Generator().manual_seed(300 + seed)
+    total = int(sum(chunks))
+    q = torch.randn(total, cfg.q_heads, 128, generator=g).to(cfg.qdt)
+    starts = torch.tensor([0] + list(np.cumsum(chunks)), dtype=torch.int32)
+    out = torch.full((total, cfg.q_heads, 128), float("nan"), dtype=_DT[out_dtype], device="cuda")
+    pkv.pkv_paged_prefill_attention(run.desc, q.cuda(), run.k_cache, run.v_cache, run.tables,
+                                    run.ctx, starts.cuda(),
+                                    max(chunks) if max_q_len is None else max_q_len,
+                                    cfg.softmax_scale, out)
+    torch.cuda.synchronize()
+    return q, starts, out
+
+
+def _expected(w, cfg, q, starts, chunks, pairs=None):
+    """Oracle rows for (sequence, query head) pairs (all when None)."""
+    ref = {}
+    grp = cfg.group
+    for b, n in enumerate(chunks):
+        if n == 0:
+            continue
+        for hq in range(cfg.q_heads):
+            if pairs is not None and (b, hq) not in pairs:
+                continue
+            K, V = logical_kv_fp64(w, b, hq // grp)
+            qq = q[int(starts[b]):int(starts[b]) + n, hq].double().numpy()
+            ref[(b, hq)] = oracle.multi_query_decode(qq, K, V, cfg.softmax_scale)
+    return ref
+
+
+@pytest.mark.parametrize("case", [
+    # name, Hq, Hkv, cache, ctx, chunk rows, out dtype
+    ("g4_bf16", 8, 2, "bf16", [1, 17, 300, 700, 129], [1, 17, 130, 256, 128], "f32"),
+    ("g1_f16", 4, 4, "f16", [40, 513, 260], [40, 200, 3], "f32"),
+    ("g8_bf16_out16", 16, 2, "bf16", [1000, 64], [300, 64], "bf16"),
+    ("g2_f16_out16", 4, 2, "f16", [2050, 16], [129, 5], "f16"),
+])
+def test_prefill_matches_the_oracle(case):
+    name, Hq, Hkv, cache, ctx, chunks, out_dtype = case
+    cfg, w, run = _setup(name, Hq, Hkv, cache, ctx, 61)
+    q, starts, out = _prefill(run, cfg, chunks, out_dtype)
+    assert run.err_code() == 0
+    ref = _expected(w, cfg, q, starts, chunks)
+    got = out.double().cpu().numpy()
+    for (b, hq), r in ref.items():
+        s0 = int(starts[b])
+        assert_close(got[s0:s0 + chunks[b], hq], r, cfg, out_dtype, f"{name} b{b} h{hq}")
+
+
+def test_prefill_long_chunk_sampled_and_deterministic():
+    """A 1024-row chunk over a 4096-token context (8 row tiles, 32 token
+    blocks for the last tile): sampled heads against the oracle, and a second
+    run bit for bit equal to the first."""
+    cfg, w, run = _setup("long", 8, 2, "bf16", [4096, 1500], 62)
+    chunks = [1024, 700]
+    q, starts, out = _prefill(run, cfg, chunks, "f32", seed=1)
+    _, _, out2 = _prefill(run, cfg, chunks, "f32", seed=1)
+    assert run.err_code() == 0
+    assert torch.equal(out, out2)
+    pairs = {(0, 0), (0, 5), (1, 3)}
+    ref = _expected(w, cfg, q, starts, chunks, pairs)
+    got = out.double().cpu().numpy()
+    for (b, hq), r in ref.items():
+        s0 = int(starts[b])
+        assert_close(got[s0:s0 + chunks[b], hq], r, cfg, "f32", f"long b{b} h{hq}")
+
+
+def test_prefill_one_row_equals_decode():
+    """A chunk of one row per sequence is the decode step's attention row."""
+    cfg, w, run = _setup("one", 8, 2, "bf16", [1, 33, 900], 63)
+    dec = run.decode("f32")
+    starts = torch.arange(4, dtype=torch.int32)
+    out = torch.empty(3, 8, 128, dtype=torch.float32, device="cuda")
+    pkv.pkv_paged_prefill_attention(run.desc, run.q, run.k_cache, run.v_cache, run.tables,
+                                    run.ctx, starts.cuda(), 1, cfg.softmax_scale, out)
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    assert (out - dec).abs().max().item() < 1e-3
+
+
+def test_prefill_bad_rows_are_reported_not_computed():
+    cfg, w, run = _setup("bad", 8, 2, "bf16", [20, 50], 64)
+    # sequence 0 claims 30 rows but holds only 20 positions
+    q = torch.zeros(40, 8, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((40, 8, 128), 7.0, dtype=torch.float32, device="cuda")
+    starts = torch.tensor([0, 30, 40], dtype=torch.int32, device="cuda")
+    pkv.pkv_paged_prefill_attention(run.desc, q, run.k_cache, run.v_cache, run.tables,
+                                    run.ctx, starts, 30, cfg.softmax_scale, out)
+    torch.cuda.synchronize()
+    assert run.err_code() == pkv.PKV_ERR_BOUNDS
+    assert torch.all(out[:30] == 7.0)          # sequence 0 untouched
+    assert torch.all(torch.isfinite(out[30:]))  # sequence 1 computed
+
+
+def test_prefill_unsupported_shapes():
+    cfg = wl.small_config("fp8", 2, 8, 2, 128, "e4m3", 1, seed=65)
+    w = wl.generate(cfg, ctx_override=torch.tensor([10, 20]))
+    run = GpuRun(w)
+    q = torch.zeros(4, 8, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(4, 8, 128, dtype=torch.float32, device="cuda")
+    starts = torch.tensor([0, 2, 4], dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_paged_prefill_attention(run.desc, q, run.k_cache, run.v_cache, run.tables,
+                                        run.ctx, starts, 2, cfg.softmax_scale, out)
