@@ -475,7 +475,8 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   if (fn == nullptr) return PKV_ERR_CUDA;
   const cuuint64_t dims[3] = {128, (cuuint64_t)desc->num_q_heads, (cuuint64_t)total_q};
   const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)desc->num_q_heads * 128 * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const int G = desc->num_q_heads / desc->num_kv_heads;  // a box: 128 / G tokens x G heads
+  const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
   const cuuint32_t estr[3] = {1, 1, 1};
   if (fn(&l.tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -492,7 +493,7 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   l.p.NB = desc->num_blocks;
   l.p.MBS = max_blocks_per_seq;
   l.p.total_q = total_q;
-  l.p.tiles_per_seq = (max_q_len + 127) / 128;
+  l.p.tiles_per_seq = (max_q_len + 128 / G - 1) / (128 / G);
   l.p.out_dtype = out_dtype;
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.bf16 = desc->cache_dtype == PKV_BF16;

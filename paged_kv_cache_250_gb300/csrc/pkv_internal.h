@@ -151,8 +151,8 @@ struct CopyParams {
 
 cudaError_t launch_copy_blocks(const CopyParams& c, int32_t n, cudaStream_t stream);
 
-// Paged prefill (pkv_prefill.cu): one CTA per 128 query rows of one
-// (sequence, query head).
+// Paged prefill (pkv_prefill.cu): one CTA per 128 query rows, 128 / g new
+// tokens of one sequence times the g query heads of one KV head.
 struct PrefillParams {
   const int32_t* q_start;       // [B+1] first query row of each sequence
   const int32_t* context_lens;  // [B]
@@ -165,7 +165,7 @@ struct PrefillParams {
 };
 struct PrefillLaunch {
   PrefillParams p;
-  CUtensorMap tmap_q;  // [total_q][Hq][128], boxes of 128 rows x 64 columns
+  CUtensorMap tmap_q;  // [total_q][Hq][128], boxes of 128 / g tokens x g heads x 64
   CUtensorMap tmap_k;  // the cache maps of the decode kernel
   CUtensorMap tmap_v;
   bool bf16;
