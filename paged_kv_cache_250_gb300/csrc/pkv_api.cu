@@ -493,7 +493,7 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   l.p.NB = desc->num_blocks;
   l.p.MBS = max_blocks_per_seq;
   l.p.total_q = total_q;
-  l.p.tiles_per_seq = (max_q_len + 128 / G - 1) / (128 / G);
+  l.p.tiles_per_seq = (max_q_len + 256 / G - 1) / (256 / G);  // a CTA: 256 / G tokens
   l.p.out_dtype = out_dtype;
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.bf16 = desc->cache_dtype == PKV_BF16;

@@ -151,7 +151,7 @@ struct CopyParams {
 
 cudaError_t launch_copy_blocks(const CopyParams& c, int32_t n, cudaStream_t stream);
 
-// Paged prefill (pkv_prefill.cu): one CTA per 128 query rows, 128 / g new
+// Paged prefill (pkv_prefill.cu): one CTA per 256 query rows, 256 / g new
 // tokens of one sequence times the g query heads of one KV head.
 struct PrefillParams {
   const int32_t* q_start;       // [B+1] first query row of each sequence

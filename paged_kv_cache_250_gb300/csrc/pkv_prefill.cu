@@ -7,23 +7,28 @@
 // chunked prefill reads each sequence's pages through its table).  Token j of
 // the chunk sits at position ctx - q_len + j and sees positions 0 .. itself.
 //
-// One CTA (4 warps) owns 128 query rows: 128 / g new tokens of one sequence
-// times the g query heads that share one KV head, so every page it loads
-// serves the whole group.  Row r is token r / g, head r % g.  Thread t owns
-// row t: TMEM lane t holds its scores and its output accumulator, so the
-// online softmax (running max m, sum l, rescale of O) needs no shuffles.
-// Per block of 64 cached tokens (4 pages):
+// One CTA owns 256 query rows in two tiles of 128: 256 / g new tokens of one
+// sequence times the g query heads that share one KV head, so every page it
+// loads serves the whole group and both tiles.  In a tile, row r is token
+// r / g, head r % g.  The CTA's warps have fixed roles:
+//   warps 0-3, 4-7  softmax of tile 0, tile 1: thread t of the group owns row
+//                   t, TMEM lane t, so the online softmax (running max m, sum
+//                   l, rescale of O) needs no shuffles;
+//   warp 8          issues the MMAs (one thread);
+//   warp 9          issues the tensor copies (one thread).
+// Per block of 64 cached tokens (4 pages), for each tile:
 //   S = Q K^T    tcgen05.mma, M 128 x N 64 x K 128 (d), both operands K-major
 //                128-byte-swizzled tiles as the tensor copies write them;
-//   softmax      tcgen05.ld of the thread's row, mask, exp2, P as a bf16 (or
-//                fp16) hi + lo pair written to shared memory;
+//   softmax      tcgen05.ld of the row, mask, exp2, P as a bf16 (or fp16)
+//                hi + lo pair written to shared memory;
 //   O += P V     tcgen05.mma twice (hi and lo), M 128 x N 128 (d) x K 64
 //                (tokens); V is used where the copies put it, as an MN-major
 //                operand.
-// K and V have one buffer each: the next block's K is copied in while this
-// block's softmax runs, its V once this block's P.V is done.  About 97 KB of
-// shared memory and 256 TMEM columns let two CTAs share an SM, so one CTA's
-// MMAs and copies overlap the other's softmax.
+// The MMA thread alternates between the tiles (P.V of one, then the next
+// block's scores of the same tile), so the tensor cores work on one tile while
+// the other tile's softmax runs.  K and V blocks are double-buffered.  The
+// roles hand over through mbarriers only; tensor memory holds S0, S1 (64
+// columns each) and O0, O1 (128 each), all 512 columns.
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -32,21 +37,24 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfRows = 128;          // query rows per CTA
+constexpr int kPfRows = 128;          // query rows per tile; two tiles per CTA
 constexpr int kPfTok = 64;            // cached tokens per block (4 pages)
 constexpr int kPfPages = kPfTok / kPageSize;
 constexpr int kPfD = 128;             // head dim built
-constexpr int kPfThreads = 128;
+constexpr int kPfThreads = 320;       // 8 softmax warps, the MMA warp, the copy warp
 constexpr uint32_t kQHalf = 16384;    // 128 rows x 128 bytes: d columns 0-63 or 64-127 of Q
 constexpr uint32_t kKHalf = 8192;     // 64 rows x 128 bytes: the same of a K or V block
 // shared memory plan, offsets from a 1024-byte aligned base
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = 2 * kQHalf;
-constexpr uint32_t kOffV = kOffK + 2 * kKHalf;
-constexpr uint32_t kOffPh = kOffV + 2 * kKHalf;  // P: 128 rows x 64 tokens, hi then lo
-constexpr uint32_t kOffPl = kOffPh + kQHalf;
-constexpr uint32_t kOffBar = kOffPl + kQHalf;    // mbarriers q, k, v, s, o; TMEM base; counts
-constexpr uint32_t kTmemCols = 256;              // S: columns 0..63, O: 128..255
+constexpr uint32_t kOffQ = 0;                    // tile t at t * 2 * kQHalf
+constexpr uint32_t kOffK = 4 * kQHalf;           // buffer b at b * 2 * kKHalf
+constexpr uint32_t kOffV = kOffK + 4 * kKHalf;
+constexpr uint32_t kOffP = kOffV + 4 * kKHalf;   // tile t: hi at t * 2 * kQHalf, lo after it
+constexpr uint32_t kOffBar = kOffP + 4 * kQHalf;
+// mbarriers (8 bytes each) from kOffBar
+constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKFree = 5, kBarVFree = 7,
+              kBarSFull = 9, kBarPFull = 11, kBarODone = 13, kNumBars = 15;
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort flag, counts
+constexpr uint32_t kTmemCols = 512;  // S0 0..63, S1 64..127, O0 128..255, O1 256..383
 constexpr uint64_t kPfWaitNs = 1000000000ull;
 
 __device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const void* tmap, uint32_t bar,
@@ -129,284 +137,329 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kPfThreads, 2)
+__global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   const int b = blockIdx.x / p.tiles_per_seq;
-  const int tile = blockIdx.x - b * p.tiles_per_seq;
+  const int ctile = blockIdx.x - b * p.tiles_per_seq;
   const int h = blockIdx.y;                 // KV head
   const int G = p.Hq / p.Hkv;               // query heads per KV head
   const int tpt = kPfRows / G;              // tokens per tile
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int q0 = p.q_start[b], qn = p.q_start[b + 1] - q0;  // this sequence's rows
   const int ctx = p.context_lens[b];
   if (qn < 0 || ctx < qn || ctx > p.MBS * kPageSize || q0 < 0 || q0 + qn > p.total_q ||
-      qn > p.tiles_per_seq * tpt) {
-    if (tid == 0 && tile == 0 && h == 0) report_error(p.err_word, PKV_ERR_BOUNDS);
+      qn > p.tiles_per_seq * 2 * tpt) {
+    if (tid == 0 && ctile == 0 && h == 0) report_error(p.err_word, PKV_ERR_BOUNDS);
     return;
   }
-  if (tile * tpt >= qn) return;  // no rows of this sequence in the tile
+  const int tok_base = ctile * 2 * tpt;  // first new token of the CTA
+  if (tok_base >= qn) return;            // no rows of this sequence here
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t bar_q = base + kOffBar, bar_k = bar_q + 8, bar_v = bar_q + 16,
-                 bar_s = bar_q + 24, bar_o = bar_q + 32;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + kOffBar + 40);
-  // completions expected on the q, k, v, s, o barriers (thread 0 counts)
-  volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(base_ptr + kOffBar + 44);
+  auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * (uint32_t)i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(base_ptr + kOffMisc + 4);
+  // completions expected on each barrier (counted by the thread that arms it)
+  volatile int32_t* armed = reinterpret_cast<volatile int32_t*>(base_ptr + kOffMisc + 8);
 
   if (warp == 0) {
-    tmem_alloc(base + kOffBar + 40, kTmemCols);
+    tmem_alloc(base + kOffMisc, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) issued[i] = 0;
-    for (int i = 0; i < 5; ++i) mbar_init(bar_q + 8 * i, 1);
+    *abort_flag = 0;
+    for (int i = 0; i < kNumBars; ++i) {
+      armed[i] = 0;
+      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? kPfRows : 1);
+    }
     fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_o = tmem + 128;   // column offsets
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
-  // row t of the tile: new token j = tile * tpt + t / G (position ctx - qn + j),
-  // query head h * G + t % G
-  const int row = tile * tpt + tid / G;
-  const int hq = h * G + tid % G;
-  const bool row_real = row < qn;
-  const int pos_q = ctx - qn + row;
-  const int vis = min(pos_q, ctx - 1);  // last visible position of this row
-  const int last_row = min(qn, (tile + 1) * tpt) - 1;
-  const int nblk = (ctx - qn + last_row) / kPfTok + 1;  // causal: blocks any row sees
-  const int all_vis = ctx - qn + tile * tpt;            // every row sees positions <= this
+  const int last_tok = min(qn, tok_base + 2 * tpt) - 1;
+  const int nblk = (ctx - qn + last_tok) / kPfTok + 1;  // causal: blocks any row sees
   const int np = (ctx + kPageSize - 1) / kPageSize;
-  const float c2 = p.scale_log2;
-  constexpr uint32_t kIdS = idesc_f16(BF16, false, kPfRows, kPfTok);
-  constexpr uint32_t kIdO = idesc_f16(BF16, true, kPfRows, kPfD);
 
-  // Every wait is bounded and its outcome voted on by the whole CTA, so all
-  // threads leave the loop together and every barrier is met.
-  auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-    const bool bad = !mbar_wait_bounded(bar, parity, kPfWaitNs);
-    return __syncthreads_or(bad) == 0;
-  };
-  // the tensor copies of block j's K (or V) pages; pages past the context are
-  // not loaded (their scores are masked, their V rows zeroed)
-  auto load_block = [&](int j, bool v) {
-    const uint32_t dst = base + (v ? kOffV : kOffK);
-    const uint32_t bar = v ? bar_v : bar_k;
-    const int pg0 = j * kPfPages;
-    const int npg = min(kPfPages, np - pg0);
-    issued[v ? 2 : 1] = issued[v ? 2 : 1] + 1;
-    mbar_arrive_expect_tx(bar, (uint32_t)npg * 2 * kPageSize * 128);
-    for (int i = 0; i < npg; ++i) {
-      int blk = p.block_tables[(int64_t)b * p.MBS + pg0 + i];
-      if (blk < 0 || blk >= p.NB) {  // the copy reads the fill value (zeros) past the pool
-        report_error(p.err_word, PKV_ERR_BOUNDS);
-        blk = p.NB;
-      }
-      const int r = (blk * p.Hkv + h) * kPageSize;
-      for (int c = 0; c < 2; ++c)
-        tma_load_2d_plain(dst + (uint32_t)c * kKHalf + (uint32_t)i * kPageSize * 128,
-                          v ? (const void*)&tmv : (const void*)&tmk, bar, c * 64, r);
-    }
+  // A bounded wait; a wait that gives up raises the CTA's abort flag, and
+  // every role stops waiting once the flag is up, so no role can stall the
+  // others for more than one bound.
+  auto wait = [&](int i, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar(i), parity, kPfWaitNs)) return true;
+    *abort_flag = 1;
+    return false;
   };
 
-  if (tid == 0) {
-    prefetch_tmap(&tmq);
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-    issued[0] = 1;
-    mbar_arrive_expect_tx(bar_q, 2 * kQHalf);
-    for (int c = 0; c < 2; ++c)
-      tma_load_3d(base + kOffQ + (uint32_t)c * kQHalf, &tmq, bar_q, c * 64, h * G,
-                  q0 + tile * tpt);
-    load_block(0, false);
-    load_block(0, true);
-  }
-  bool dead = !wait_all(bar_q, 0);
-
-  float m_ref = -INFINITY, l_sum = 0.f;
-  for (int j = 0; j < nblk && !dead; ++j) {
-    const uint32_t par = (uint32_t)(j & 1);
-    if (!wait_all(bar_k, par)) {
-      dead = true;
-      break;
-    }
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < kPfD / 16; ++ks) {  // S = Q K^T over d, 16 at a time
-        const uint32_t qoff = (uint32_t)(ks >> 2) * kQHalf + (uint32_t)(ks & 3) * 32;
-        const uint32_t koff = (uint32_t)(ks >> 2) * kKHalf + (uint32_t)(ks & 3) * 32;
-        umma(t_s, sdesc(base + kOffQ + qoff, 16, 1024), sdesc(base + kOffK + koff, 16, 1024),
-             kIdS, ks > 0);
-      }
-      issued[3] = issued[3] + 1;
-      umma_commit(bar_s);
-    }
-    if (!wait_all(bar_s, par)) {
-      dead = true;
-      break;
-    }
-    tc_fence_after();
-    if (tid == 0 && j + 1 < nblk) load_block(j + 1, false);  // K is free again
-
-    // ---- softmax of this thread's row (log2 domain), masked past `vis`
-    const int tok0 = j * kPfTok;
-    const bool full = tok0 + kPfTok - 1 <= all_vis;  // no row masks anything here
-    uint32_t r[32];
-    float mx = -INFINITY;
-#pragma unroll 1
-    for (int cc = 0; cc < kPfTok / 32; ++cc) {
-      tmem_ld32(t_s + lane_base + (uint32_t)cc * 32, r);
-      if (full) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (tok0 + cc * 32 + e <= vis) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
-      }
-    }
-    // lazy rescale: keep the reference max while scores stay within 2^8 of it
-    const bool grow = mx > m_ref + 8.f;
-    float alpha = 1.f;
-    if (grow) {
-      alpha = ex2(m_ref - mx);  // 0 on the first block
-      m_ref = mx;
-      l_sum *= alpha;
-    }
-    if (j > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const uint32_t ta = t_o + lane_base + (uint32_t)cc * 32;
-        tmem_ld32(ta, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-        tmem_st32(ta, r);
-      }
-    }
-    const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-#pragma unroll 1
-    for (int cc = 0; cc < kPfTok / 32; ++cc) {
-      tmem_ld32(t_s + lane_base + (uint32_t)cc * 32, r);
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float p0 = ex2(__uint_as_float(r[e]) * c2 - mu);
-        float p1 = ex2(__uint_as_float(r[e + 1]) * c2 - mu);
-        if (!full) {
-          const int t = tok0 + cc * 32 + e;
-          if (t > vis) p0 = 0.f;
-          if (t + 1 > vis) p1 = 0.f;
-        }
-        l_sum += p0 + p1;
-        hi[e / 2] = pack2<BF16>(p0, p1);
-        const float2 f = unpack2<BF16>(hi[e / 2]);
-        lo[e / 2] = pack2<BF16>(p0 - f.x, p1 - f.y);
-      }
-      // row tid, tokens cc*32 .. +31: four 16-byte chunks of the swizzled row
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = cc * 4 + q;
-        const uint32_t off = (uint32_t)tid * 128 + (uint32_t)((chunk ^ (tid & 7)) * 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + kOffPh + off),
-                     "r"(hi[4 * q]), "r"(hi[4 * q + 1]), "r"(hi[4 * q + 2]), "r"(hi[4 * q + 3])
-                     : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + kOffPl + off),
-                     "r"(lo[4 * q]), "r"(lo[4 * q + 1]), "r"(lo[4 * q + 2]), "r"(lo[4 * q + 3])
-                     : "memory");
-      }
-    }
-    if (!wait_all(bar_v, par)) {  // block j's V (copied while S and the softmax ran)
-      dead = true;
-      break;
-    }
-    // rows of V past the context hold whatever the pool or an older block left:
-    // zero them (the MMA multiplies them by P = 0)
-    if (tok0 + kPfTok > ctx) {
-      const int first = max(0, ctx - tok0);
-      for (int i = tid; i < (kPfTok - first) * 16; i += kPfThreads) {
-        const int rr = first + i / 16, ch = i % 16;  // row, 16-byte chunk of the row
-        const uint32_t a = base + kOffV + (uint32_t)(ch >> 3) * kKHalf + (uint32_t)rr * 128 +
-                           (uint32_t)(ch & 7) * 16;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
-      }
-    }
-    // P and the zeroed V rows are read by the tensor cores (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < kPfTok / 16; ++ks) {  // O += P V over tokens, 16 at a time
-        const uint64_t bv = sdesc(base + kOffV + (uint32_t)ks * 16 * 128, kKHalf, 1024);
-        umma(t_o, sdesc(base + kOffPh + (uint32_t)ks * 32, 16, 1024), bv, kIdO, j > 0 || ks > 0);
-        umma(t_o, sdesc(base + kOffPl + (uint32_t)ks * 32, 16, 1024), bv, kIdO, 1);
-      }
-      issued[4] = issued[4] + 1;
-      umma_commit(bar_o);
-    }
-    if (!wait_all(bar_o, par)) {
-      dead = true;
-      break;
-    }
-    tc_fence_after();
-    if (tid == 0 && j + 1 < nblk) load_block(j + 1, true);  // V is free again
-  }
-
-  // ---- out = O / l for the tile's real rows
-  if (!dead) {
-    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    const int64_t orow = ((int64_t)(q0 + row) * p.Hq + hq) * kPfD;
-    uint32_t r[32];
-#pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      tmem_ld32(t_o + lane_base + (uint32_t)cc * 32, r);
-      if (row_real) {
-        if (p.out_dtype == PKV_F32) {
-          float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + cc * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o4[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                __uint_as_float(r[4 * e + 2]) * inv,
-                                __uint_as_float(r[4 * e + 3]) * inv);
-        } else {
-          uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow + cc * 32);
-          const bool obf = p.out_dtype == PKV_BF16;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float a = __uint_as_float(r[8 * e + 2 * k]) * inv;
-              const float c = __uint_as_float(r[8 * e + 2 * k + 1]) * inv;
-              w[k] = obf ? pack2<true>(a, c) : pack2<false>(a, c);
+  if (warp == 9) {
+    // ---------------------------------------------------------- copies
+    if (lane == 0) {
+      prefetch_tmap(&tmq);
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+      armed[kBarQ] = 1;
+      mbar_arrive_expect_tx(bar(kBarQ), 4 * kQHalf);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(base + kOffQ + (uint32_t)(t * 2 + c) * kQHalf, &tmq, bar(kBarQ), c * 64,
+                      h * G, q0 + tok_base + t * tpt);
+      for (int j = 0; j < nblk; ++j) {
+        const int bb = j & 1;
+        const int pg0 = j * kPfPages;
+        const int npg = min(kPfPages, np - pg0);
+        for (int v = 0; v < 2; ++v) {  // K, then V of block j
+          const int full = (v ? kBarVFull : kBarKFull) + bb;
+          if (j >= 2 && !wait((v ? kBarVFree : kBarKFree) + bb, (uint32_t)(((j - 2) >> 1) & 1)))
+            break;
+          armed[full] = armed[full] + 1;
+          mbar_arrive_expect_tx(bar(full), (uint32_t)npg * 2 * kPageSize * 128);
+          const uint32_t dst = base + (v ? kOffV : kOffK) + (uint32_t)bb * 2 * kKHalf;
+          for (int i = 0; i < npg; ++i) {
+            int blk = p.block_tables[(int64_t)b * p.MBS + pg0 + i];
+            if (blk < 0 || blk >= p.NB) {  // the copy reads the fill value (zeros) past the pool
+              report_error(p.err_word, PKV_ERR_BOUNDS);
+              blk = p.NB;
             }
-            o4[e] = make_uint4(w[0], w[1], w[2], w[3]);
+            const int r = (blk * p.Hkv + h) * kPageSize;
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d_plain(dst + (uint32_t)c * kKHalf + (uint32_t)i * kPageSize * 128,
+                                v ? (const void*)&tmv : (const void*)&tmk, bar(full), c * 64, r);
           }
+        }
+        if (*abort_flag) break;
+      }
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------- MMAs
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(BF16, false, kPfRows, kPfTok);
+      constexpr uint32_t kIdO = idesc_f16(BF16, true, kPfRows, kPfD);
+      auto commit = [&](int i) {
+        armed[i] = armed[i] + 1;
+        umma_commit(bar(i));
+      };
+      auto qk = [&](int t, int j) {  // S_t = Q_t K(j)^T over d, 16 at a time
+        const uint32_t kb = base + kOffK + (uint32_t)(j & 1) * 2 * kKHalf;
+#pragma unroll
+        for (int ks = 0; ks < kPfD / 16; ++ks) {
+          const uint32_t qoff = (uint32_t)(t * 2 + (ks >> 2)) * kQHalf + (uint32_t)(ks & 3) * 32;
+          const uint32_t koff = (uint32_t)(ks >> 2) * kKHalf + (uint32_t)(ks & 3) * 32;
+          umma(tmem + (uint32_t)t * kPfTok, sdesc(base + kOffQ + qoff, 16, 1024),
+               sdesc(kb + koff, 16, 1024), kIdS, ks > 0);
+        }
+        commit(kBarSFull + t);
+      };
+      auto pv = [&](int t, int j) {  // O_t += P_t V(j) over tokens, 16 at a time
+        const uint32_t vb = base + kOffV + (uint32_t)(j & 1) * 2 * kKHalf;
+        const uint32_t ph = base + kOffP + (uint32_t)t * 2 * kQHalf, pl = ph + kQHalf;
+        const uint32_t dt = tmem + 128 + (uint32_t)t * kPfD;
+#pragma unroll
+        for (int ks = 0; ks < kPfTok / 16; ++ks) {
+          const uint64_t bv = sdesc(vb + (uint32_t)ks * 16 * 128, kKHalf, 1024);
+          umma(dt, sdesc(ph + (uint32_t)ks * 32, 16, 1024), bv, kIdO, j > 0 || ks > 0);
+          umma(dt, sdesc(pl + (uint32_t)ks * 32, 16, 1024), bv, kIdO, 1);
+        }
+        commit(kBarODone + t);
+      };
+      bool ok = wait(kBarQ, 0) && wait(kBarKFull, 0);
+      if (ok) {
+        tc_fence_after();
+        qk(0, 0);
+        qk(1, 0);
+        commit(kBarKFree);
+      }
+      for (int j = 0; ok && j < nblk; ++j) {
+        const int bb = j & 1, nb = (j + 1) & 1;
+        const uint32_t par = (uint32_t)(j & 1);
+        if (!wait(kBarPFull, par) || !wait(kBarVFull + bb, (uint32_t)((j >> 1) & 1))) break;
+        tc_fence_after();
+        pv(0, j);
+        const bool more = j + 1 < nblk;
+        if (more) {
+          if (!wait(kBarKFull + nb, (uint32_t)(((j + 1) >> 1) & 1))) break;
+          qk(0, j + 1);
+        }
+        if (!wait(kBarPFull + 1, par)) break;
+        tc_fence_after();
+        pv(1, j);
+        commit(kBarVFree + bb);
+        if (more) {
+          qk(1, j + 1);
+          commit(kBarKFree + nb);
         }
       }
     }
   } else {
-    // a wait gave up: let this CTA's copies and MMAs land (bounded, each
-    // barrier's last expected phase) before the tensor memory is released
-    if (tid == 0) report_error(p.err_word, PKV_ERR_TIMEOUT);
-    for (int i = 0; i < 5; ++i)
-      if (issued[i] > 0)
-        mbar_wait_bounded(bar_q + 8 * i, (uint32_t)((issued[i] - 1) & 1), kPfWaitNs);
+    // ---------------------------------------------------------- softmax
+    const int t = warp >> 2;             // tile
+    const int tt = tid - t * kPfRows;    // row in the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + (uint32_t)t * kPfTok + lane_base;
+    const uint32_t t_o = tmem + 128 + (uint32_t)t * kPfD + lane_base;
+    const uint32_t ph = base + kOffP + (uint32_t)t * 2 * kQHalf, pl = ph + kQHalf;
+    const int row = tok_base + t * tpt + tt / G;  // new token of this row
+    const int hq = h * G + tt % G;
+    const bool row_real = row < qn;
+    const int vis = min(ctx - qn + row, ctx - 1);        // last visible position
+    const int all_vis = ctx - qn + tok_base + t * tpt;   // every row of the tile sees <= this
+    const float c2 = p.scale_log2;
+    float m_ref = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    uint32_t r[32];
+    for (int j = 0; j < nblk; ++j) {
+      const uint32_t par = (uint32_t)(j & 1);
+      ok = __all_sync(0xffffffffu, wait(kBarSFull + t, par));
+      if (!ok) break;
+      tc_fence_after();
+      const int tok0 = j * kPfTok;
+      const bool full = tok0 + kPfTok - 1 <= all_vis;  // no row masks anything here
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < kPfTok / 32; ++cc) {
+        tmem_ld32(t_s + (uint32_t)cc * 32, r);
+        if (full) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (tok0 + cc * 32 + e <= vis) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
+        }
+      }
+      // lazy rescale: keep the reference max while scores stay within 2^8 of it
+      const bool grow = mx > m_ref + 8.f;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - mx);  // 0 on the first block
+        m_ref = mx;
+        l_sum *= alpha;
+      }
+      if (j > 0) {  // O_t and P_t are free once the previous block's P.V is done
+        ok = __all_sync(0xffffffffu, wait(kBarODone + t, (uint32_t)((j - 1) & 1)));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t ta = t_o + (uint32_t)cc * 32;
+            tmem_ld32(ta, r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(ta, r);
+          }
+        }
+      }
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll 1
+      for (int cc = 0; cc < kPfTok / 32; ++cc) {
+        tmem_ld32(t_s + (uint32_t)cc * 32, r);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2(__uint_as_float(r[e]) * c2 - mu);
+          float p1 = ex2(__uint_as_float(r[e + 1]) * c2 - mu);
+          if (!full) {
+            const int tk = tok0 + cc * 32 + e;
+            if (tk > vis) p0 = 0.f;
+            if (tk + 1 > vis) p1 = 0.f;
+          }
+          l_sum += p0 + p1;
+          hi[e / 2] = pack2<BF16>(p0, p1);
+          const float2 f = unpack2<BF16>(hi[e / 2]);
+          lo[e / 2] = pack2<BF16>(p0 - f.x, p1 - f.y);
+        }
+        // row tt, tokens cc*32 .. +31: four 16-byte chunks of the swizzled row
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = cc * 4 + q;
+          const uint32_t off = (uint32_t)tt * 128 + (uint32_t)((chunk ^ (tt & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off),
+                       "r"(hi[4 * q]), "r"(hi[4 * q + 1]), "r"(hi[4 * q + 2]),
+                       "r"(hi[4 * q + 3]) : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pl + off),
+                       "r"(lo[4 * q]), "r"(lo[4 * q + 1]), "r"(lo[4 * q + 2]),
+                       "r"(lo[4 * q + 3]) : "memory");
+        }
+      }
+      // rows of V past the context hold whatever the pool or an older block
+      // left: tile 0 zeroes them before it hands over (the MMA multiplies them
+      // by P = 0)
+      if (t == 0 && tok0 + kPfTok > ctx) {
+        ok = __all_sync(0xffffffffu, wait(kBarVFull + (j & 1), (uint32_t)((j >> 1) & 1)));
+        if (!ok) break;
+        const int first = max(0, ctx - tok0);
+        const uint32_t vb = base + kOffV + (uint32_t)(j & 1) * 2 * kKHalf;
+        for (int i = tt; i < (kPfTok - first) * 16; i += kPfRows) {
+          const int rr = first + i / 16, ch = i % 16;  // row, 16-byte chunk of the row
+          const uint32_t a = vb + (uint32_t)(ch >> 3) * kKHalf + (uint32_t)rr * 128 +
+                             (uint32_t)(ch & 7) * 16;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+        }
+      }
+      // P (and zeroed V rows) are read by the tensor cores (async proxy); S_t
+      // reads are done
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull + t));
+    }
+    // ---- out = O / l for the tile's real rows
+    if (ok) ok = __all_sync(0xffffffffu, wait(kBarODone + t, (uint32_t)((nblk - 1) & 1)));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const int64_t orow = ((int64_t)(q0 + row) * p.Hq + hq) * kPfD;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(t_o + (uint32_t)cc * 32, r);
+        if (row_real) {
+          if (p.out_dtype == PKV_F32) {
+            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + cc * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o4[e] = make_float4(__uint_as_float(r[4 * e]) * inv,
+                                  __uint_as_float(r[4 * e + 1]) * inv,
+                                  __uint_as_float(r[4 * e + 2]) * inv,
+                                  __uint_as_float(r[4 * e + 3]) * inv);
+          } else {
+            uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow + cc * 32);
+            const bool obf = p.out_dtype == PKV_BF16;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float a = __uint_as_float(r[8 * e + 2 * k]) * inv;
+                const float c = __uint_as_float(r[8 * e + 2 * k + 1]) * inv;
+                w[k] = obf ? pack2<true>(a, c) : pack2<false>(a, c);
+              }
+              o4[e] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
   }
+
+  // ---- every role is done.  After an abort, let this CTA's copies and MMAs
+  // land (bounded, each barrier's last armed phase) before the tensor memory
+  // is released.
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    if (tid == 0) report_error(p.err_word, PKV_ERR_TIMEOUT);
+    if (tid < kNumBars && tid != kBarPFull && tid != kBarPFull + 1 && armed[tid] > 0)
+      mbar_wait_bounded(bar(tid), (uint32_t)((armed[tid] - 1) & 1), kPfWaitNs);
+    __syncthreads();
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -415,7 +468,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
 }  // namespace
 
-size_t prefill_smem_bytes() { return 1024 + kOffBar + 64; }
+size_t prefill_smem_bytes() { return 1024 + kOffMisc + 8 + 4 * kNumBars; }
 
 cudaError_t launch_prefill(const PrefillLaunch& l) {
   const size_t smem = prefill_smem_bytes();
