@@ -129,6 +129,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
                :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
@@ -177,7 +183,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     *abort_flag = 0;
     for (int i = 0; i < kNumBars; ++i) {
       armed[i] = 0;
-      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? kPfRows : 1);
+      // P full: one arrival per softmax warp of the tile
+      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? kPfRows / 32 : 1);
     }
     fence_mbar_init();
   }
@@ -247,26 +254,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         armed[i] = armed[i] + 1;
         umma_commit(bar(i));
       };
+      // The descriptors' address field is (address >> 4) in 14 bits and shared
+      // memory ends below 256 KB, so a descriptor at address + offset is the
+      // base descriptor plus offset >> 4: build the bases once.
+      const uint64_t dq = sdesc(base + kOffQ, 16, 1024);
+      const uint64_t dk = sdesc(base + kOffK, 16, 1024);
+      const uint64_t dv = sdesc(base + kOffV, kKHalf, 1024);
+      const uint64_t dp = sdesc(base + kOffP, 16, 1024);
       auto qk = [&](int t, int j) {  // S_t = Q_t K(j)^T over d, 16 at a time
-        const uint32_t kb = base + kOffK + (uint32_t)(j & 1) * 2 * kKHalf;
+        const uint64_t a0 = dq + ((uint64_t)t * 2 * kQHalf >> 4);
+        const uint64_t b0 = dk + ((uint64_t)(j & 1) * 2 * kKHalf >> 4);
 #pragma unroll
         for (int ks = 0; ks < kPfD / 16; ++ks) {
-          const uint32_t qoff = (uint32_t)(t * 2 + (ks >> 2)) * kQHalf + (uint32_t)(ks & 3) * 32;
+          const uint32_t qoff = (uint32_t)(ks >> 2) * kQHalf + (uint32_t)(ks & 3) * 32;
           const uint32_t koff = (uint32_t)(ks >> 2) * kKHalf + (uint32_t)(ks & 3) * 32;
-          umma(tmem + (uint32_t)t * kPfTok, sdesc(base + kOffQ + qoff, 16, 1024),
-               sdesc(kb + koff, 16, 1024), kIdS, ks > 0);
+          umma(tmem + (uint32_t)t * kPfTok, a0 + (qoff >> 4), b0 + (koff >> 4), kIdS, ks > 0);
         }
         commit(kBarSFull + t);
       };
       auto pv = [&](int t, int j) {  // O_t += P_t V(j) over tokens, 16 at a time
-        const uint32_t vb = base + kOffV + (uint32_t)(j & 1) * 2 * kKHalf;
-        const uint32_t ph = base + kOffP + (uint32_t)t * 2 * kQHalf, pl = ph + kQHalf;
+        const uint64_t b0 = dv + ((uint64_t)(j & 1) * 2 * kKHalf >> 4);
+        const uint64_t ah = dp + ((uint64_t)t * 2 * kQHalf >> 4), al = ah + (kQHalf >> 4);
         const uint32_t dt = tmem + 128 + (uint32_t)t * kPfD;
 #pragma unroll
         for (int ks = 0; ks < kPfTok / 16; ++ks) {
-          const uint64_t bv = sdesc(vb + (uint32_t)ks * 16 * 128, kKHalf, 1024);
-          umma(dt, sdesc(ph + (uint32_t)ks * 32, 16, 1024), bv, kIdO, j > 0 || ks > 0);
-          umma(dt, sdesc(pl + (uint32_t)ks * 32, 16, 1024), bv, kIdO, 1);
+          const uint64_t bv = b0 + ((uint32_t)ks * 16 * 128 >> 4);
+          umma(dt, ah + (ks * 32 >> 4), bv, kIdO, j > 0 || ks > 0);
+          umma(dt, al + (ks * 32 >> 4), bv, kIdO, 1);
         }
         commit(kBarODone + t);
       };
@@ -277,25 +291,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         qk(1, 0);
         commit(kBarKFree);
       }
+      // Per tile: the next block's scores go to the tensor cores before this
+      // block's P.V, so the tile's softmax can take its row maxima while the
+      // P.V runs (it waits for "O done" only when it reaches O and P).
       for (int j = 0; ok && j < nblk; ++j) {
         const int bb = j & 1, nb = (j + 1) & 1;
         const uint32_t par = (uint32_t)(j & 1);
-        if (!wait(kBarPFull, par) || !wait(kBarVFull + bb, (uint32_t)((j >> 1) & 1))) break;
-        tc_fence_after();
-        pv(0, j);
         const bool more = j + 1 < nblk;
+        if (!wait(kBarPFull, par)) break;  // S0 read, P0 written
+        tc_fence_after();
         if (more) {
           if (!wait(kBarKFull + nb, (uint32_t)(((j + 1) >> 1) & 1))) break;
           qk(0, j + 1);
         }
+        if (!wait(kBarVFull + bb, (uint32_t)((j >> 1) & 1))) break;
+        pv(0, j);
         if (!wait(kBarPFull + 1, par)) break;
         tc_fence_after();
-        pv(1, j);
-        commit(kBarVFree + bb);
         if (more) {
           qk(1, j + 1);
           commit(kBarKFree + nb);
         }
+        pv(1, j);
+        commit(kBarVFree + bb);
       }
     }
   } else {
@@ -314,7 +332,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const float c2 = p.scale_log2;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
-    uint32_t r[32];
+    uint32_t r[32], sr[kPfTok];
     for (int j = 0; j < nblk; ++j) {
       const uint32_t par = (uint32_t)(j & 1);
       ok = __all_sync(0xffffffffu, wait(kBarSFull + t, par));
@@ -323,17 +341,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int tok0 = j * kPfTok;
       const bool full = tok0 + kPfTok - 1 <= all_vis;  // no row masks anything here
       float mx = -INFINITY;
-#pragma unroll 1
-      for (int cc = 0; cc < kPfTok / 32; ++cc) {
-        tmem_ld32(t_s + (uint32_t)cc * 32, r);
-        if (full) {
+      tmem_ld64(t_s, sr);  // the row's 64 scores stay in registers for both passes
+      if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
-        } else {
+        for (int e = 0; e < kPfTok; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (tok0 + cc * 32 + e <= vis) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
-        }
+        for (int e = 0; e < kPfTok; ++e)
+          if (tok0 + e <= vis) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
       }
       // lazy rescale: keep the reference max while scores stay within 2^8 of it
       const bool grow = mx > m_ref + 8.f;
@@ -359,14 +374,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-#pragma unroll 1
+#pragma unroll
       for (int cc = 0; cc < kPfTok / 32; ++cc) {
-        tmem_ld32(t_s + (uint32_t)cc * 32, r);
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(__uint_as_float(r[e]) * c2 - mu);
-          float p1 = ex2(__uint_as_float(r[e + 1]) * c2 - mu);
+          float p0 = ex2(__uint_as_float(sr[cc * 32 + e]) * c2 - mu);
+          float p1 = ex2(__uint_as_float(sr[cc * 32 + e + 1]) * c2 - mu);
           if (!full) {
             const int tk = tok0 + cc * 32 + e;
             if (tk > vis) p0 = 0.f;
@@ -409,7 +423,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // reads are done
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPFull + t));
     }
     // ---- out = O / l for the tile's real rows
     if (ok) ok = __all_sync(0xffffffffu, wait(kBarODone + t, (uint32_t)((nblk - 1) & 1)));
