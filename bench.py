@@ -423,10 +423,17 @@ def committed_traffic(workload):
     return ent.get("dram_bytes_per_launch")
 
 
+# the sources the decode and append kernels are built from (the prefill and
+# block-copy kernels do not change them)
+DECODE_SOURCES = ("pkv_decode_impl.cuh", "pkv_device.cuh", "pkv_internal.h", "pkv_api.cu",
+                  "pkv_append.cu", "pkv_decode_bf16.cu", "pkv_decode_f16.cu", "pkv_decode_e4m3.cu",
+                  "pkv_decode_e4m3_tok.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_250_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in DECODE_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
