@@ -112,3 +112,62 @@ def test_argument_errors_return_before_any_launch():
                                         float("nan"), fake, pkv.PKV_BF16, pkv.PKV_BF16, fake,
                                         1 << 20, None)
     assert st == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_argument_errors_of_the_later_entry_points():
+    """Window, multi-query, one-kernel step, prefill and the per-token FP8
+    descriptor: argument errors found on the host, before any CUDA call."""
+    lib = pkv.load_library()
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    good = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_BF16)
+    D = ctypes.byref(good)
+    # sliding window: negative window or sinks, q_len 0
+    for q_len, window, sinks in ((1, -1, 0), (1, 8, -2), (0, 8, 0)):
+        st = lib.pkv_paged_decode_attention_window(D, fake, fake, fake, fake, fake, 2, q_len,
+                                                   window, sinks, 4, 0, 1.0, fake, pkv.PKV_BF16,
+                                                   pkv.PKV_F32, fake, 1 << 20, None)
+        assert st == pkv.PKV_ERR_INVALID_ARG
+    # multi-query: q_len 0; more (token, head) columns than the 8 built
+    st = lib.pkv_paged_decode_attention_multi(D, fake, fake, fake, fake, fake, 2, 0, 4, 0, 1.0,
+                                              fake, pkv.PKV_BF16, pkv.PKV_F32, fake, 1 << 20, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    st = lib.pkv_paged_decode_attention_multi(D, fake, fake, fake, fake, fake, 2, 3, 4, 0, 1.0,
+                                              fake, pkv.PKV_BF16, pkv.PKV_F32, fake, 1 << 20, None)
+    assert st == pkv.PKV_ERR_UNSUPPORTED  # group 4 x 3 tokens > 8
+    # one-kernel step: a null q; an empty batch is a no-op
+    st = lib.pkv_decode_step_fused(D, None, fake, fake, fake, fake, pkv.PKV_BF16, fake, fake, 2,
+                                   4, 0, 1.0, fake, pkv.PKV_BF16, pkv.PKV_F32, fake, 1 << 20, 0,
+                                   None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_fused(D, None, None, None, None, None, pkv.PKV_BF16, None, None,
+                                     0, 4, 0, 1.0, None, pkv.PKV_BF16, pkv.PKV_F32, None, 0, 0,
+                                     None) == pkv.PKV_OK
+    # prefill: FP8 caches and head_dim 64 are not built; q must match the cache;
+    # negative sizes; empty calls are no-ops
+    fp8 = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_FP8_E4M3)
+    fp8.k_scale = fp8.v_scale = 0x1000
+    d64 = pkv.make_desc(64, 16, 2, 8, 64, pkv.PKV_BF16)
+
+    def prefill(desc, q_dtype=pkv.PKV_BF16, batch=2, total=8, maxq=4):
+        return lib.pkv_paged_prefill_attention(ctypes.byref(desc), fake, fake, fake, fake, fake,
+                                               fake, batch, total, maxq, 4, 1.0, fake, q_dtype,
+                                               pkv.PKV_F32, None)
+    assert prefill(fp8) == pkv.PKV_ERR_UNSUPPORTED
+    assert prefill(d64) == pkv.PKV_ERR_UNSUPPORTED
+    assert prefill(good, q_dtype=pkv.PKV_F16) == pkv.PKV_ERR_INVALID_ARG
+    assert prefill(good, total=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert prefill(good, batch=0) == pkv.PKV_OK
+    assert prefill(good, maxq=0) == pkv.PKV_OK
+    # per-token FP8: the scale pool must be 128-byte aligned; v_scale is unused
+    tok = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_FP8_E4M3_TOKEN)
+    tok.k_scale = 0x1040  # 64-byte aligned only
+    st = lib.pkv_kv_append(ctypes.byref(tok), fake, fake, fake, fake, fake, 1, pkv.PKV_BF16, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    tok.k_scale = 0x1080
+    assert lib.pkv_kv_append(ctypes.byref(tok), None, None, None, None, None, 0, pkv.PKV_BF16,
+                             None) == pkv.PKV_OK
+    tok64 = pkv.make_desc(64, 16, 2, 8, 64, pkv.PKV_FP8_E4M3_TOKEN)
+    tok64.k_scale = 0x1080
+    st = lib.pkv_kv_append(ctypes.byref(tok64), fake, fake, fake, fake, fake, 1, pkv.PKV_BF16,
+                           None)
+    assert st == pkv.PKV_ERR_UNSUPPORTED
