@@ -16,19 +16,21 @@
 //                   l, rescale of O) needs no shuffles;
 //   warp 8          issues the MMAs (one thread);
 //   warp 9          issues the tensor copies (one thread).
-// Per block of 64 cached tokens (4 pages), for each tile:
-//   S = Q K^T    tcgen05.mma, M 128 x N 64 x K 128 (d), both operands K-major
-//                128-byte-swizzled tiles as the tensor copies write them;
+// Per block of 128 cached tokens (8 pages), for each tile:
+//   S = Q K^T    tcgen05.mma, M 128 x N 128 x K 128 (d), both operands K-major
+//                128-byte-swizzled tiles as the tensor copies write them, the
+//                scores landing in tensor memory;
 //   softmax      tcgen05.ld of the row, mask, exp2, P as a bf16 (or fp16)
-//                hi + lo pair written to shared memory;
-//   O += P V     tcgen05.mma twice (hi and lo), M 128 x N 128 (d) x K 64
-//                (tokens); V is used where the copies put it, as an MN-major
-//                operand.
-// The MMA thread alternates between the tiles (P.V of one, then the next
-// block's scores of the same tile), so the tensor cores work on one tile while
-// the other tile's softmax runs.  K and V blocks are double-buffered.  The
-// roles hand over through mbarriers only; tensor memory holds S0, S1 (64
-// columns each) and O0, O1 (128 each), all 512 columns.
+//                hi + lo pair written back over the row's scores (tcgen05.st);
+//   O += P V     tcgen05.mma with A read from tensor memory, twice (hi and lo)
+//                per 64 tokens, M 128 x N 128 (d) x K 16 per instruction; V is
+//                used where the copies put it, as an MN-major operand.
+// The MMA thread alternates between the tiles (P.V of one tile, then the next
+// block's scores of the same tile, which overwrite its P: MMAs run in issue
+// order), so the tensor cores work on one tile while the other tile's softmax
+// runs.  K and V blocks are double-buffered.  The roles hand over through
+// mbarriers only; tensor memory holds S0/P0, S1/P1, O0 and O1, 128 columns
+// each.
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -38,23 +40,22 @@ namespace pkv {
 namespace {
 
 constexpr int kPfRows = 128;          // query rows per tile; two tiles per CTA
-constexpr int kPfTok = 64;            // cached tokens per block (4 pages)
+constexpr int kPfTok = 128;           // cached tokens per block (8 pages)
 constexpr int kPfPages = kPfTok / kPageSize;
 constexpr int kPfD = 128;             // head dim built
 constexpr int kPfThreads = 320;       // 8 softmax warps, the MMA warp, the copy warp
 constexpr uint32_t kQHalf = 16384;    // 128 rows x 128 bytes: d columns 0-63 or 64-127 of Q
-constexpr uint32_t kKHalf = 8192;     // 64 rows x 128 bytes: the same of a K or V block
+constexpr uint32_t kKHalf = 16384;    // 128 rows x 128 bytes: the same of a K or V block
 // shared memory plan, offsets from a 1024-byte aligned base
 constexpr uint32_t kOffQ = 0;                    // tile t at t * 2 * kQHalf
 constexpr uint32_t kOffK = 4 * kQHalf;           // buffer b at b * 2 * kKHalf
 constexpr uint32_t kOffV = kOffK + 4 * kKHalf;
-constexpr uint32_t kOffP = kOffV + 4 * kKHalf;   // tile t: hi at t * 2 * kQHalf, lo after it
-constexpr uint32_t kOffBar = kOffP + 4 * kQHalf;
+constexpr uint32_t kOffBar = kOffV + 4 * kKHalf;
 // mbarriers (8 bytes each) from kOffBar
 constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKFree = 5, kBarVFree = 7,
               kBarSFull = 9, kBarPFull = 11, kBarODone = 13, kNumBars = 15;
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort flag, counts
-constexpr uint32_t kTmemCols = 512;  // S0 0..63, S1 64..127, O0 128..255, O1 256..383
+constexpr uint32_t kTmemCols = 512;  // S0/P0 0..127, S1/P1 128..255, O0 256..383, O1 384..511
 constexpr uint64_t kPfWaitNs = 1000000000ull;
 
 __device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const void* tmap, uint32_t bar,
@@ -99,6 +100,15 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem]^T, kind::f16: A is M lanes x K 16-bit values,
+// two per 32-bit column
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 // arrive once on `bar` when every MMA this thread issued before has completed
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -260,7 +270,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint64_t dq = sdesc(base + kOffQ, 16, 1024);
       const uint64_t dk = sdesc(base + kOffK, 16, 1024);
       const uint64_t dv = sdesc(base + kOffV, kKHalf, 1024);
-      const uint64_t dp = sdesc(base + kOffP, 16, 1024);
       auto qk = [&](int t, int j) {  // S_t = Q_t K(j)^T over d, 16 at a time
         const uint64_t a0 = dq + ((uint64_t)t * 2 * kQHalf >> 4);
         const uint64_t b0 = dk + ((uint64_t)(j & 1) * 2 * kKHalf >> 4);
@@ -272,15 +281,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         commit(kBarSFull + t);
       };
-      auto pv = [&](int t, int j) {  // O_t += P_t V(j) over tokens, 16 at a time
+      // O_t += P_t V(j) over tokens, 16 at a time; P_t sits over S_t's
+      // columns: per 64 tokens, 32 columns of hi pairs, then 32 of lo pairs
+      auto pv = [&](int t, int j) {
         const uint64_t b0 = dv + ((uint64_t)(j & 1) * 2 * kKHalf >> 4);
-        const uint64_t ah = dp + ((uint64_t)t * 2 * kQHalf >> 4), al = ah + (kQHalf >> 4);
-        const uint32_t dt = tmem + 128 + (uint32_t)t * kPfD;
+        const uint32_t pt = tmem + (uint32_t)t * kPfTok;
+        const uint32_t dt = tmem + 256 + (uint32_t)t * kPfD;
 #pragma unroll
         for (int ks = 0; ks < kPfTok / 16; ++ks) {
           const uint64_t bv = b0 + ((uint32_t)ks * 16 * 128 >> 4);
-          umma(dt, ah + (ks * 32 >> 4), bv, kIdO, j > 0 || ks > 0);
-          umma(dt, al + (ks * 32 >> 4), bv, kIdO, 1);
+          const uint32_t pa = pt + (uint32_t)(ks >> 2) * 64 + (uint32_t)(ks & 3) * 8;
+          umma_ts(dt, pa, bv, kIdO, j > 0 || ks > 0);
+          umma_ts(dt, pa + 32, bv, kIdO, 1);
         }
         commit(kBarODone + t);
       };
@@ -291,29 +303,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         qk(1, 0);
         commit(kBarKFree);
       }
-      // Per tile: the next block's scores go to the tensor cores before this
-      // block's P.V, so the tile's softmax can take its row maxima while the
-      // P.V runs (it waits for "O done" only when it reaches O and P).
+      // Per tile: this block's P.V, then the next block's scores, which
+      // overwrite P (the MMAs of one thread run in issue order).
       for (int j = 0; ok && j < nblk; ++j) {
         const int bb = j & 1, nb = (j + 1) & 1;
         const uint32_t par = (uint32_t)(j & 1);
         const bool more = j + 1 < nblk;
-        if (!wait(kBarPFull, par)) break;  // S0 read, P0 written
+        if (!wait(kBarPFull, par)) break;  // P0 written over S0
+        if (!wait(kBarVFull + bb, (uint32_t)((j >> 1) & 1))) break;
         tc_fence_after();
+        pv(0, j);
         if (more) {
           if (!wait(kBarKFull + nb, (uint32_t)(((j + 1) >> 1) & 1))) break;
           qk(0, j + 1);
         }
-        if (!wait(kBarVFull + bb, (uint32_t)((j >> 1) & 1))) break;
-        pv(0, j);
         if (!wait(kBarPFull + 1, par)) break;
         tc_fence_after();
+        pv(1, j);
+        commit(kBarVFree + bb);
         if (more) {
           qk(1, j + 1);
           commit(kBarKFree + nb);
         }
-        pv(1, j);
-        commit(kBarVFree + bb);
       }
     }
   } else {
@@ -321,9 +332,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int t = warp >> 2;             // tile
     const int tt = tid - t * kPfRows;    // row in the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + (uint32_t)t * kPfTok + lane_base;
-    const uint32_t t_o = tmem + 128 + (uint32_t)t * kPfD + lane_base;
-    const uint32_t ph = base + kOffP + (uint32_t)t * 2 * kQHalf, pl = ph + kQHalf;
+    const uint32_t t_s = tmem + (uint32_t)t * kPfTok + lane_base;  // S_t, then P_t
+    const uint32_t t_o = tmem + 256 + (uint32_t)t * kPfD + lane_base;
     const int row = tok_base + t * tpt + tt / G;  // new token of this row
     const int hq = h * G + tt % G;
     const bool row_real = row < qn;
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const float c2 = p.scale_log2;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
-    uint32_t r[32], sr[kPfTok];
+    uint32_t r[32], sr[64];
     for (int j = 0; j < nblk; ++j) {
       const uint32_t par = (uint32_t)(j & 1);
       ok = __all_sync(0xffffffffu, wait(kBarSFull + t, par));
@@ -341,14 +351,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int tok0 = j * kPfTok;
       const bool full = tok0 + kPfTok - 1 <= all_vis;  // no row masks anything here
       float mx = -INFINITY;
-      tmem_ld64(t_s, sr);  // the row's 64 scores stay in registers for both passes
-      if (full) {
+#pragma unroll 1
+      for (int th = 0; th < 2; ++th) {  // the row's 128 scores, 64 at a time
+        tmem_ld64(t_s + (uint32_t)th * 64, sr);
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < kPfTok; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
-      } else {
+          for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+        } else {
 #pragma unroll
-        for (int e = 0; e < kPfTok; ++e)
-          if (tok0 + e <= vis) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+          for (int e = 0; e < 64; ++e)
+            if (tok0 + th * 64 + e <= vis) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+        }
       }
       // lazy rescale: keep the reference max while scores stay within 2^8 of it
       const bool grow = mx > m_ref + 8.f;
@@ -374,15 +387,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      // P over S: per 64 tokens, the hi pairs (32 columns) then the lo pairs;
+      // the scores of a half are read before its columns are written
+#pragma unroll 1
+      for (int th = 0; th < 2; ++th) {
+        tmem_ld64(t_s + (uint32_t)th * 64, sr);
+        uint32_t hi[32], lo[32];
 #pragma unroll
-      for (int cc = 0; cc < kPfTok / 32; ++cc) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(__uint_as_float(sr[cc * 32 + e]) * c2 - mu);
-          float p1 = ex2(__uint_as_float(sr[cc * 32 + e + 1]) * c2 - mu);
+        for (int e = 0; e < 64; e += 2) {
+          float p0 = ex2(__uint_as_float(sr[e]) * c2 - mu);
+          float p1 = ex2(__uint_as_float(sr[e + 1]) * c2 - mu);
           if (!full) {
-            const int tk = tok0 + cc * 32 + e;
+            const int tk = tok0 + th * 64 + e;
             if (tk > vis) p0 = 0.f;
             if (tk + 1 > vis) p1 = 0.f;
           }
@@ -391,18 +407,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float2 f = unpack2<BF16>(hi[e / 2]);
           lo[e / 2] = pack2<BF16>(p0 - f.x, p1 - f.y);
         }
-        // row tt, tokens cc*32 .. +31: four 16-byte chunks of the swizzled row
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = cc * 4 + q;
-          const uint32_t off = (uint32_t)tt * 128 + (uint32_t)((chunk ^ (tt & 7)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off),
-                       "r"(hi[4 * q]), "r"(hi[4 * q + 1]), "r"(hi[4 * q + 2]),
-                       "r"(hi[4 * q + 3]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pl + off),
-                       "r"(lo[4 * q]), "r"(lo[4 * q + 1]), "r"(lo[4 * q + 2]),
-                       "r"(lo[4 * q + 3]) : "memory");
-        }
+        tmem_st32(t_s + (uint32_t)th * 64, hi);
+        tmem_st32(t_s + (uint32_t)th * 64 + 32, lo);
       }
       // rows of V past the context hold whatever the pool or an older block
       // left: tile 0 zeroes them before it hands over (the MMA multiplies them
@@ -419,8 +425,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
         }
       }
-      // P (and zeroed V rows) are read by the tensor cores (async proxy); S_t
-      // reads are done
+      // zeroed V rows are read by the tensor cores (async proxy); P is in
+      // tensor memory
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
