@@ -237,6 +237,28 @@ class Step:
                             self.out, self.ws, self.hint, stream=stream)
 
 
+class Staging:
+    """A step's host inputs packed at 256-byte aligned offsets of one pinned
+    buffer, with a device twin: one copy moves them all, and the step reads
+    device views into the twin (the layout a caller staging its inputs would
+    use)."""
+
+    def __init__(self, tensors, device):
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(total, dtype=torch.uint8, device=device)
+        self.views = []
+        self.payload_bytes = 0
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            self.payload_bytes += n
+            self.host[o:o + n].copy_(t.detach().contiguous().view(-1).view(torch.uint8).cpu())
+            self.views.append(self.dev[o:o + n].view(t.dtype).view(t.shape))
+
+
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -299,25 +321,45 @@ def run_native(args, cfg, rank, world, device):
     g_one_plain = capture(body_one_no_overlap, stream)
     g_events = capture(body_events, stream)
 
-    # e2e: pinned host inputs copied in, output copied out, every step
-    h_q = st.q.cpu().pin_memory()
-    h_k = st.k_new.cpu().pin_memory()
-    h_v = st.v_new.cpu().pin_memory()
-    h_tab = st.tables.cpu().pin_memory()
-    h_ctx = st.ctx.cpu().pin_memory()
-    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_ctx))
-    d2h = h_out.numel() * h_out.element_size()
+    # e2e: every step copies its inputs (q, new k/v, tables, lengths) in from
+    # pinned host memory, packed in one staging buffer (one copy), runs the
+    # step on views into it, and copies its output back.  Staging and outputs
+    # are double-buffered and the copies run on their own streams, so step
+    # i + 1's inputs and step i - 1's output move while step i computes.
+    stages = [Staging([st.q, st.k_new, st.v_new, st.tables, st.ctx], device) for _ in range(2)]
+    outs = [torch.empty_like(st.out) for _ in range(2)]
+    h_outs = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
+    h2d = stages[0].host.numel()  # the bytes copied (inputs plus alignment padding)
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
     def body_e2e():
+        ev_in = [torch.cuda.Event() for _ in range(K)]
+        ev_k = [torch.cuda.Event() for _ in range(K)]
+        ev_out = [torch.cuda.Event() for _ in range(K)]
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
         for i in range(K):
-            st.q.copy_(h_q, non_blocking=True)
-            st.k_new.copy_(h_k, non_blocking=True)
-            st.v_new.copy_(h_v, non_blocking=True)
-            st.tables.copy_(h_tab, non_blocking=True)
-            st.ctx.copy_(h_ctx, non_blocking=True)
-            st.step_one(i % R, stream)
-            h_out.copy_(st.out, non_blocking=True)
+            bb = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_k[i - 2])      # step i - 2 read this staging buffer
+            with torch.cuda.stream(s_in):
+                stages[bb].dev.copy_(stages[bb].host, non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])  # step i - 2's output has left
+            sq, sk, sv, stab, sctx = stages[bb].views
+            pkv.pkv_decode_step_fused(st.desc, sq, st.kc[i % R], st.vc[i % R], sk, sv, stab, sctx,
+                                      cfg.softmax_scale, outs[bb], st.ws, st.hint, stream=stream,
+                                      overlap=True)
+            ev_k[i].record(stream)
+            s_out.wait_event(ev_k[i])
+            with torch.cuda.stream(s_out):
+                h_outs[bb].copy_(outs[bb], non_blocking=True)
+                ev_out[i].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
 
     g_e2e = capture(body_e2e, stream)
     torch.cuda.synchronize(device)
@@ -401,7 +443,12 @@ def run_native(args, cfg, rank, world, device):
                      "peak_kind": peak_kind},
         "e2e": {"value": round(whole_job_gbps(step_bytes, ms_e2e / K, world), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(ms_e2e / K, 5)},
+                "ms_per_step": round(ms_e2e / K, 5),
+                "method": "each step: one host-to-device copy of the step's inputs packed in a "
+                          "pinned staging buffer, the step on views into its device twin, one "
+                          "device-to-host copy of the output; double-buffered, the copies on their "
+                          "own streams overlapping the neighbouring steps; all inside the timed "
+                          "graph"},
         "gpu_launches": K,
         "clocks": clocks,
     }
