@@ -150,7 +150,7 @@ class GpuRun:
                             out, self.workspace, self.hint)
         return out
 
-    def step_one_kernel(self, out_dtype: str = "f32") -> torch.Tensor:
+    def step_one_kernel(self, out_dtype: str = "f32", overlap: bool = False) -> torch.Tensor:
         """One decode step as a single kernel (pkv_decode_step_fused): each new
         row lands at its sequence's newest position."""
         cfg = self.w.cfg
@@ -158,7 +158,7 @@ class GpuRun:
                           device=self.dev)
         pkv.pkv_decode_step_fused(self.desc, self.q, self.k_cache, self.v_cache, self.k_new,
                                   self.v_new, self.tables, self.ctx, cfg.softmax_scale, out,
-                                  self.workspace, self.hint)
+                                  self.workspace, self.hint, overlap=overlap)
         return out
 
     def err_code(self) -> int:

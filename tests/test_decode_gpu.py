@@ -299,3 +299,26 @@ def test_full_size_configs_sampled(name):
     assert_close(np.stack([out32[b, hq] for b, hq in pairs]), r, cfg, "f32", name)
     assert_close(np.stack([out[b, hq] for b, hq in pairs]), r, cfg,
                  "bf16" if cfg.cache != "f16" else "f16", name)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_timed_step_sampled(name):
+    """Every full-size workload through the call the bench times
+    (pkv_decode_step_fused with PKV_STEP_OVERLAP), sampled rows against the
+    oracle, 16-bit output."""
+    cfg = wl.CONFIGS[name]
+    w = wl.generate(cfg, device="cuda")
+    run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
+    odt = "bf16" if cfg.cache != "f16" else "f16"
+    out = run.step_one_kernel(odt, overlap=True).double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    assert np.all(np.isfinite(out))
+    rng = np.random.default_rng(cfg.seed + 17)
+    ctx = w.ctx.numpy()
+    bs = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), cfg.batch - 1,
+                 *rng.integers(0, cfg.batch, 3).tolist()})
+    pairs = [(b, int(hq)) for b in bs for hq in rng.choice(cfg.q_heads, 2, replace=False)]
+    ref = oracle_rows(w, pairs)
+    assert_close(np.stack([out[b, hq] for b, hq in pairs]), np.stack([ref[p] for p in pairs]),
+                 cfg, odt, name)
