@@ -257,6 +257,7 @@ PKV_API pkv_status pkv_decode_step(
  *   max_q_len     host: an upper bound on q_start[b + 1] - q_start[b]; it
  *                 sizes the launch.
  *   context_lens  tokens of each sequence, the chunk included (>= n_b).
+ *   scale         > 0 (the softmax scale); otherwise PKV_ERR_INVALID_ARG.
  *   out           [total_q][num_q_heads][128] of out_dtype (F16 | BF16 | F32).
  * A sequence whose rows, length or table break these rules is a device-
  * detected PKV_ERR_BOUNDS; its output rows are then not written.  No

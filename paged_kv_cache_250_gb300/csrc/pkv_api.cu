@@ -459,7 +459,7 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   if (q_dtype != desc->cache_dtype) return PKV_ERR_INVALID_ARG;
   if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
     return PKV_ERR_UNSUPPORTED;
-  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return PKV_ERR_INVALID_ARG;  // the kernel takes row maxima unscaled
   if ((int64_t)batch * max_blocks_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
   if ((int64_t)max_blocks_per_seq * kPageSize >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
   if ((int64_t)total_q * desc->num_q_heads >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;

@@ -350,19 +350,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_fence_after();
       const int tok0 = j * kPfTok;
       const bool full = tok0 + kPfTok - 1 <= all_vis;  // no row masks anything here
-      float mx = -INFINITY;
+      // row max of the raw scores (c2 > 0 commutes with the max), in four
+      // independent chains
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
       for (int th = 0; th < 2; ++th) {  // the row's 128 scores, 64 at a time
         tmem_ld64(t_s + (uint32_t)th * 64, sr);
         if (full) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+          for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
         } else {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (tok0 + th * 64 + e <= vis) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+            if (tok0 + th * 64 + e <= vis) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
         }
       }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
       // lazy rescale: keep the reference max while scores stay within 2^8 of it
       const bool grow = mx > m_ref + 8.f;
       float alpha = 1.f;
@@ -393,20 +396,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int th = 0; th < 2; ++th) {
         tmem_ld64(t_s + (uint32_t)th * 64, sr);
         uint32_t hi[32], lo[32];
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          float p0 = ex2(__uint_as_float(sr[e]) * c2 - mu);
-          float p1 = ex2(__uint_as_float(sr[e + 1]) * c2 - mu);
+          float p0 = ex2(fmaf(__uint_as_float(sr[e]), c2, -mu));
+          float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), c2, -mu));
           if (!full) {
             const int tk = tok0 + th * 64 + e;
             if (tk > vis) p0 = 0.f;
             if (tk + 1 > vis) p1 = 0.f;
           }
-          l_sum += p0 + p1;
+          l4[(e >> 1) & 3] += p0 + p1;
           hi[e / 2] = pack2<BF16>(p0, p1);
           const float2 f = unpack2<BF16>(hi[e / 2]);
           lo[e / 2] = pack2<BF16>(p0 - f.x, p1 - f.y);
         }
+        l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_st32(t_s + (uint32_t)th * 64, hi);
         tmem_st32(t_s + (uint32_t)th * 64 + 32, lo);
       }
