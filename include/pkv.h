@@ -249,8 +249,8 @@ PKV_API pkv_status pkv_decode_step(
  * sequence b's chunk sits at position context_lens[b] - n_b + j (n_b its
  * row count) and attends to positions 0 .. that position.  Runs on the
  * tensor cores (tcgen05, accumulators in tensor memory); 16-bit caches with
- * head_dim 128 (others return PKV_ERR_UNSUPPORTED).
- *   q             [total_q][num_q_heads][128] of q_dtype (= cache_dtype);
+ * head_dim 64 or 128 (others return PKV_ERR_UNSUPPORTED).
+ *   q             [total_q][num_q_heads][head_dim] of q_dtype (= cache_dtype);
  *                 sequence b's rows are q_start[b] .. q_start[b + 1] - 1.
  *   q_start       int32 [batch + 1], device, non-decreasing, q_start[batch]
  *                 <= total_q.
@@ -258,7 +258,8 @@ PKV_API pkv_status pkv_decode_step(
  *                 sizes the launch.
  *   context_lens  tokens of each sequence, the chunk included (>= n_b).
  *   scale         > 0 (the softmax scale); otherwise PKV_ERR_INVALID_ARG.
- *   out           [total_q][num_q_heads][128] of out_dtype (F16 | BF16 | F32).
+ *   out           [total_q][num_q_heads][head_dim] of out_dtype (F16 | BF16 |
+ *                 F32).
  * A sequence whose rows, length or table break these rules is a device-
  * detected PKV_ERR_BOUNDS; its output rows are then not written.  No
  * workspace.  Inputs are read after the preceding kernel on the stream

@@ -331,7 +331,7 @@ def pkv_paged_prefill_attention(desc: CacheDesc, q: torch.Tensor, k_cache: torch
                                 context_lens: torch.Tensor, q_start: torch.Tensor,
                                 max_q_len: int, scale: float, out: torch.Tensor,
                                 stream=None) -> None:
-    """q/out: [total_q][Hq][128]; sequence b's rows q_start[b] .. q_start[b+1]-1
+    """q/out: [total_q][Hq][d]; sequence b's rows q_start[b] .. q_start[b+1]-1
     are its last positions, causal; q_start int32 [B+1] on the device."""
     lib = load_library()
     for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),

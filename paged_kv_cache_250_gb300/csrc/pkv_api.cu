@@ -455,7 +455,7 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !q_start || !out)
     return PKV_ERR_INVALID_ARG;
   if (desc->cache_dtype != PKV_F16 && desc->cache_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (desc->head_dim != 64 && desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (q_dtype != desc->cache_dtype) return PKV_ERR_INVALID_ARG;
   if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
     return PKV_ERR_UNSUPPORTED;
@@ -473,8 +473,9 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   if (st != PKV_OK) return st;
   auto fn = encode_fn();
   if (fn == nullptr) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {128, (cuuint64_t)desc->num_q_heads, (cuuint64_t)total_q};
-  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)desc->num_q_heads * 128 * 2};
+  const cuuint64_t hd = (cuuint64_t)desc->head_dim;
+  const cuuint64_t dims[3] = {hd, (cuuint64_t)desc->num_q_heads, (cuuint64_t)total_q};
+  const cuuint64_t strides[2] = {hd * 2, (cuuint64_t)desc->num_q_heads * hd * 2};
   const int G = desc->num_q_heads / desc->num_kv_heads;  // a box: 128 / G tokens x G heads
   const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
   const cuuint32_t estr[3] = {1, 1, 1};
@@ -497,6 +498,7 @@ pkv_status pkv_paged_prefill_attention(const pkv_cache_desc* desc, const void* q
   l.p.out_dtype = out_dtype;
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.bf16 = desc->cache_dtype == PKV_BF16;
+  l.d = desc->head_dim;
   l.stream = reinterpret_cast<cudaStream_t>(stream);
   if ((int64_t)batch * l.p.tiles_per_seq >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
   return pkv::launch_prefill(l) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

@@ -157,7 +157,7 @@ struct PrefillParams {
   const int32_t* q_start;       // [B+1] first query row of each sequence
   const int32_t* context_lens;  // [B]
   const int32_t* block_tables;  // [B][MBS]
-  void* out;                    // [total_q][Hq][128]
+  void* out;                    // [total_q][Hq][d]
   int32_t* err_word;
   int32_t B, Hq, Hkv, NB, MBS, total_q, tiles_per_seq;
   pkv_dtype out_dtype;
@@ -165,13 +165,14 @@ struct PrefillParams {
 };
 struct PrefillLaunch {
   PrefillParams p;
-  CUtensorMap tmap_q;  // [total_q][Hq][128], boxes of 128 / g tokens x g heads x 64
+  CUtensorMap tmap_q;  // [total_q][Hq][d], boxes of 128 / g tokens x g heads x 64
   CUtensorMap tmap_k;  // the cache maps of the decode kernel
   CUtensorMap tmap_v;
   bool bf16;
+  int32_t d;           // head dim: 64 or 128
   cudaStream_t stream;
 };
-size_t prefill_smem_bytes();
+size_t prefill_smem_bytes(int d);
 cudaError_t launch_prefill(const PrefillLaunch& l);
 
 }  // namespace pkv

@@ -42,20 +42,27 @@ namespace {
 constexpr int kPfRows = 128;          // query rows per tile; two tiles per CTA
 constexpr int kPfTok = 128;           // cached tokens per block (8 pages)
 constexpr int kPfPages = kPfTok / kPageSize;
-constexpr int kPfD = 128;             // head dim built
 constexpr int kPfThreads = 320;       // 8 softmax warps, the MMA warp, the copy warp
-constexpr uint32_t kQHalf = 16384;    // 128 rows x 128 bytes: d columns 0-63 or 64-127 of Q
+constexpr uint32_t kQHalf = 16384;    // 128 rows x 128 bytes: 64 d columns of a Q tile
 constexpr uint32_t kKHalf = 16384;    // 128 rows x 128 bytes: the same of a K or V block
-// shared memory plan, offsets from a 1024-byte aligned base
-constexpr uint32_t kOffQ = 0;                    // tile t at t * 2 * kQHalf
-constexpr uint32_t kOffK = 4 * kQHalf;           // buffer b at b * 2 * kKHalf
-constexpr uint32_t kOffV = kOffK + 4 * kKHalf;
-constexpr uint32_t kOffBar = kOffV + 4 * kKHalf;
-// mbarriers (8 bytes each) from kOffBar
+// mbarriers (8 bytes each) from the barrier area
 constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKFree = 5, kBarVFree = 7,
               kBarSFull = 9, kBarPFull = 11, kBarODone = 13, kNumBars = 15;
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort flag, counts
-constexpr uint32_t kTmemCols = 512;  // S0/P0 0..127, S1/P1 128..255, O0 256..383, O1 384..511
+constexpr uint32_t kTmemCols = 512;  // S0/P0 0..127, S1/P1 128..255, O0 from 256, O1 after it
+// Shared memory plan for head dim D (NH = D / 64 halves of 128-byte rows),
+// offsets from a 1024-byte aligned base: Q tile t at t * NH * kQHalf, K and V
+// buffer b at b * NH * kKHalf from their areas, then barriers and counts.
+template <int D>
+struct PfPlan {
+  static constexpr int NH = D / 64;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = 2 * NH * kQHalf;
+  static constexpr uint32_t kOffV = kOffK + 2 * NH * kKHalf;
+  static constexpr uint32_t kOffBar = kOffV + 2 * NH * kKHalf;
+  static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort, counts
+  static constexpr size_t kSmem = 1024 + kOffMisc + 8 + 4 * kNumBars;
+  static_assert(D == 64 || D == 128, "head dims built");
+};
 constexpr uint64_t kPfWaitNs = 1000000000ull;
 
 __device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const void* tmap, uint32_t bar,
@@ -152,7 +159,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
@@ -163,6 +170,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int G = p.Hq / p.Hkv;               // query heads per KV head
   const int tpt = kPfRows / G;              // tokens per tile
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  using PL = PfPlan<D>;
+  constexpr int NH = PL::NH, kPfD = D;
+  constexpr uint32_t kOffQ = PL::kOffQ, kOffK = PL::kOffK, kOffV = PL::kOffV,
+                     kOffBar = PL::kOffBar, kOffMisc = PL::kOffMisc;
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int q0 = p.q_start[b], qn = p.q_start[b + 1] - q0;  // this sequence's rows
@@ -224,10 +235,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
       armed[kBarQ] = 1;
-      mbar_arrive_expect_tx(bar(kBarQ), 4 * kQHalf);
+      mbar_arrive_expect_tx(bar(kBarQ), 2 * NH * kQHalf);
       for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(base + kOffQ + (uint32_t)(t * 2 + c) * kQHalf, &tmq, bar(kBarQ), c * 64,
+        for (int c = 0; c < NH; ++c)
+          tma_load_3d(base + kOffQ + (uint32_t)(t * NH + c) * kQHalf, &tmq, bar(kBarQ), c * 64,
                       h * G, q0 + tok_base + t * tpt);
       for (int j = 0; j < nblk; ++j) {
         const int bb = j & 1;
@@ -238,8 +249,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (j >= 2 && !wait((v ? kBarVFree : kBarKFree) + bb, (uint32_t)(((j - 2) >> 1) & 1)))
             break;
           armed[full] = armed[full] + 1;
-          mbar_arrive_expect_tx(bar(full), (uint32_t)npg * 2 * kPageSize * 128);
-          const uint32_t dst = base + (v ? kOffV : kOffK) + (uint32_t)bb * 2 * kKHalf;
+          mbar_arrive_expect_tx(bar(full), (uint32_t)npg * NH * kPageSize * 128);
+          const uint32_t dst = base + (v ? kOffV : kOffK) + (uint32_t)bb * NH * kKHalf;
           for (int i = 0; i < npg; ++i) {
             int blk = p.block_tables[(int64_t)b * p.MBS + pg0 + i];
             if (blk < 0 || blk >= p.NB) {  // the copy reads the fill value (zeros) past the pool
@@ -247,7 +258,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               blk = p.NB;
             }
             const int r = (blk * p.Hkv + h) * kPageSize;
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < NH; ++c)
               tma_load_2d_plain(dst + (uint32_t)c * kKHalf + (uint32_t)i * kPageSize * 128,
                                 v ? (const void*)&tmv : (const void*)&tmk, bar(full), c * 64, r);
           }
@@ -271,8 +282,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint64_t dk = sdesc(base + kOffK, 16, 1024);
       const uint64_t dv = sdesc(base + kOffV, kKHalf, 1024);
       auto qk = [&](int t, int j) {  // S_t = Q_t K(j)^T over d, 16 at a time
-        const uint64_t a0 = dq + ((uint64_t)t * 2 * kQHalf >> 4);
-        const uint64_t b0 = dk + ((uint64_t)(j & 1) * 2 * kKHalf >> 4);
+        const uint64_t a0 = dq + ((uint64_t)t * NH * kQHalf >> 4);
+        const uint64_t b0 = dk + ((uint64_t)(j & 1) * NH * kKHalf >> 4);
 #pragma unroll
         for (int ks = 0; ks < kPfD / 16; ++ks) {
           const uint32_t qoff = (uint32_t)(ks >> 2) * kQHalf + (uint32_t)(ks & 3) * 32;
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // O_t += P_t V(j) over tokens, 16 at a time; P_t sits over S_t's
       // columns: per 64 tokens, 32 columns of hi pairs, then 32 of lo pairs
       auto pv = [&](int t, int j) {
-        const uint64_t b0 = dv + ((uint64_t)(j & 1) * 2 * kKHalf >> 4);
+        const uint64_t b0 = dv + ((uint64_t)(j & 1) * NH * kKHalf >> 4);
         const uint32_t pt = tmem + (uint32_t)t * kPfTok;
         const uint32_t dt = tmem + 256 + (uint32_t)t * kPfD;
 #pragma unroll
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_fence_after();
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < kPfD / 32; ++cc) {
             const uint32_t ta = t_o + (uint32_t)cc * 32;
             tmem_ld32(ta, r);
 #pragma unroll
@@ -422,9 +433,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = __all_sync(0xffffffffu, wait(kBarVFull + (j & 1), (uint32_t)((j >> 1) & 1)));
         if (!ok) break;
         const int first = max(0, ctx - tok0);
-        const uint32_t vb = base + kOffV + (uint32_t)(j & 1) * 2 * kKHalf;
-        for (int i = tt; i < (kPfTok - first) * 16; i += kPfRows) {
-          const int rr = first + i / 16, ch = i % 16;  // row, 16-byte chunk of the row
+        const uint32_t vb = base + kOffV + (uint32_t)(j & 1) * NH * kKHalf;
+        for (int i = tt; i < (kPfTok - first) * 8 * NH; i += kPfRows) {
+          const int rr = first + i / (8 * NH), ch = i % (8 * NH);  // row, 16-byte chunk
           const uint32_t a = vb + (uint32_t)(ch >> 3) * kKHalf + (uint32_t)rr * 128 +
                              (uint32_t)(ch & 7) * 16;
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
@@ -444,7 +455,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const int64_t orow = ((int64_t)(q0 + row) * p.Hq + hq) * kPfD;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < kPfD / 32; ++cc) {
         tmem_ld32(t_o + (uint32_t)cc * 32, r);
         if (row_real) {
           if (p.out_dtype == PKV_F32) {
@@ -494,17 +505,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 }  // namespace
 
-size_t prefill_smem_bytes() { return 1024 + kOffMisc + 8 + 4 * kNumBars; }
+size_t prefill_smem_bytes(int d) { return d == 64 ? PfPlan<64>::kSmem : PfPlan<128>::kSmem; }
 
 cudaError_t launch_prefill(const PrefillLaunch& l) {
-  const size_t smem = prefill_smem_bytes();
-  static bool configured[2] = {false, false};
-  auto kern = l.bf16 ? prefill_kernel<true> : prefill_kernel<false>;
-  if (!configured[l.bf16 ? 1 : 0]) {
+  const int d = l.d;
+  if (d != 64 && d != 128) return cudaErrorNotSupported;
+  const size_t smem = prefill_smem_bytes(d);
+  static bool configured[2][2] = {{false, false}, {false, false}};
+  auto kern = l.bf16 ? (d == 64 ? prefill_kernel<true, 64> : prefill_kernel<true, 128>)
+                     : (d == 64 ? prefill_kernel<false, 64> : prefill_kernel<false, 128>);
+  bool& done = configured[l.bf16 ? 1 : 0][d == 64 ? 0 : 1];
+  if (!done) {
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured[l.bf16 ? 1 : 0] = true;
+    done = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(l.p.B * l.p.tiles_per_seq), (unsigned)l.p.Hkv, 1);

@@ -142,18 +142,19 @@ def test_argument_errors_of_the_later_entry_points():
     assert lib.pkv_decode_step_fused(D, None, None, None, None, None, pkv.PKV_BF16, None, None,
                                      0, 4, 0, 1.0, None, pkv.PKV_BF16, pkv.PKV_F32, None, 0, 0,
                                      None) == pkv.PKV_OK
-    # prefill: FP8 caches and head_dim 64 are not built; q must match the cache;
+    # prefill: FP8 caches and head_dims other than 64 and 128 are not built; q
+    # must match the cache;
     # negative sizes; empty calls are no-ops
     fp8 = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_FP8_E4M3)
     fp8.k_scale = fp8.v_scale = 0x1000
-    d64 = pkv.make_desc(64, 16, 2, 8, 64, pkv.PKV_BF16)
+    d80 = pkv.make_desc(64, 16, 2, 8, 80, pkv.PKV_BF16)
 
     def prefill(desc, q_dtype=pkv.PKV_BF16, batch=2, total=8, maxq=4):
         return lib.pkv_paged_prefill_attention(ctypes.byref(desc), fake, fake, fake, fake, fake,
                                                fake, batch, total, maxq, 4, 1.0, fake, q_dtype,
                                                pkv.PKV_F32, None)
     assert prefill(fp8) == pkv.PKV_ERR_UNSUPPORTED
-    assert prefill(d64) == pkv.PKV_ERR_UNSUPPORTED
+    assert prefill(d80) == pkv.PKV_ERR_UNSUPPORTED
     assert prefill(good, q_dtype=pkv.PKV_F16) == pkv.PKV_ERR_INVALID_ARG
     assert prefill(good, total=-1) == pkv.PKV_ERR_INVALID_ARG
     assert prefill(good, batch=0) == pkv.PKV_OK

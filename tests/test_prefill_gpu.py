@@ -19,8 +19,8 @@ pytestmark = pytest.mark.gpu
 _DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
-def _setup(name, Hq, Hkv, cache, ctx, seed):
-    cfg = wl.small_config(name, len(ctx), Hq, Hkv, 128, cache, 1, seed=seed)
+def _setup(name, Hq, Hkv, cache, ctx, seed, d=128):
+    cfg = wl.small_config(name, len(ctx), Hq, Hkv, d, cache, 1, seed=seed)
     w = wl.generate(cfg, ctx_override=torch.tensor(ctx))
     run = GpuRun(w)
     run.append()  # every position of every sequence is now in the cache
@@ -30,9 +30,10 @@ def _setup(name, Hq, Hkv, cache, ctx, seed):
 def _prefill(run, cfg, chunks, out_dtype="f32", seed=0, max_q_len=None):
     g = torch.Generator().manual_seed(300 + seed)
     total = int(sum(chunks))
-    q = torch.randn(total, cfg.q_heads, 128, generator=g).to(cfg.qdt)
+    d = cfg.head_dim
+    q = torch.randn(total, cfg.q_heads, d, generator=g).to(cfg.qdt)
     starts = torch.tensor([0] + list(np.cumsum(chunks)), dtype=torch.int32)
-    out = torch.full((total, cfg.q_heads, 128), float("nan"), dtype=_DT[out_dtype], device="cuda")
+    out = torch.full((total, cfg.q_heads, d), float("nan"), dtype=_DT[out_dtype], device="cuda")
     pkv.pkv_paged_prefill_attention(run.desc, q.cuda(), run.k_cache, run.v_cache, run.tables,
                                     run.ctx, starts.cuda(),
                                     max(chunks) if max_q_len is None else max_q_len,
@@ -58,15 +59,17 @@ def _expected(w, cfg, q, starts, chunks, pairs=None):
 
 
 @pytest.mark.parametrize("case", [
-    # name, Hq, Hkv, cache, ctx, chunk rows, out dtype
-    ("g4_bf16", 8, 2, "bf16", [1, 17, 300, 700, 129], [1, 17, 130, 256, 128], "f32"),
-    ("g1_f16", 4, 4, "f16", [40, 513, 260], [40, 200, 3], "f32"),
-    ("g8_bf16_out16", 16, 2, "bf16", [1000, 64], [300, 64], "bf16"),
-    ("g2_f16_out16", 4, 2, "f16", [2050, 16], [129, 5], "f16"),
+    # name, Hq, Hkv, cache, ctx, chunk rows, out dtype, head dim
+    ("g4_bf16", 8, 2, "bf16", [1, 17, 300, 700, 129], [1, 17, 130, 256, 128], "f32", 128),
+    ("g1_f16", 4, 4, "f16", [40, 513, 260], [40, 200, 3], "f32", 128),
+    ("g8_bf16_out16", 16, 2, "bf16", [1000, 64], [300, 64], "bf16", 128),
+    ("g2_f16_out16", 4, 2, "f16", [2050, 16], [129, 5], "f16", 128),
+    ("g4_f16_d64", 4, 1, "f16", [256, 700, 33], [256, 300, 20], "f32", 64),
+    ("g2_bf16_d64_out16", 8, 4, "bf16", [1, 1500], [1, 390], "bf16", 64),
 ])
 def test_prefill_matches_the_oracle(case):
-    name, Hq, Hkv, cache, ctx, chunks, out_dtype = case
-    cfg, w, run = _setup(name, Hq, Hkv, cache, ctx, 61)
+    name, Hq, Hkv, cache, ctx, chunks, out_dtype, d = case
+    cfg, w, run = _setup(name, Hq, Hkv, cache, ctx, 61, d)
     q, starts, out = _prefill(run, cfg, chunks, out_dtype)
     assert run.err_code() == 0
     ref = _expected(w, cfg, q, starts, chunks)
