@@ -190,7 +190,6 @@ PKV_API pkv_status pkv_paged_decode_attention(
  *   q, out        [batch][q_len][num_q_heads][head_dim].
  *   q_len         1 .. 8 / (num_q_heads / num_kv_heads); larger returns
  *                 PKV_ERR_UNSUPPORTED.  q_len 1 is pkv_paged_decode_attention.
- *                 FP8_E4M3_TOKEN caches take q_len 1 only.
  * The workspace of pkv_decode_workspace_bytes serves any supported q_len.
  * Other arguments and guarantees as for pkv_paged_decode_attention. */
 PKV_API pkv_status pkv_paged_decode_attention_multi(

@@ -293,7 +293,7 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
       case pkv::kCacheF16: e = pkv::launch_decode_multi_f16(l); break;
       case pkv::kCacheBF16: e = pkv::launch_decode_multi_bf16(l); break;
       case pkv::kCacheE4M3: e = pkv::launch_decode_multi_e4m3(l); break;
-      default: e = cudaErrorNotSupported; break;  // per-token scales: one query token
+      default: e = pkv::launch_decode_multi_e4m3_tok(l); break;
     }
   }
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;

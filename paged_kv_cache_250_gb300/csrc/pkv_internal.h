@@ -128,6 +128,7 @@ cudaError_t launch_decode_e4m3_tok(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_e4m3(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_e4m3_tok(const DecodeLaunch& l);
 // Clears, on the stream, the parts of a decode workspace that must be zero
 // when a call begins (whatever an earlier, failed call left there).
 cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,

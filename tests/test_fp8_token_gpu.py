@@ -129,12 +129,30 @@ def test_copy_blocks_moves_the_scales():
             assert torch.equal(_bytes(a[d_]), _bytes(a[s_]))
 
 
-def test_multi_query_is_not_built_for_per_token_scales():
-    cfg = wl.small_config("tok_mq", 2, 8, 2, 128, "e4m3tok", 1, seed=100)
-    w = wl.generate(cfg, ctx_override=torch.tensor([9, 30]))
+@pytest.mark.parametrize("g,q_len", [(4, 2), (1, 8), (2, 3)])
+def test_multi_query_matches_the_oracle(g, q_len):
+    """q_len new tokens per sequence, causal among themselves, over a
+    per-token cache."""
+    cfg = wl.small_config(f"tok_mq_{g}", 4, 2 * g, 2, 128, "e4m3tok", 1, seed=100 + g)
+    w = wl.generate(cfg, ctx_override=torch.tensor([1, 9, 300, 1200]))
     run = GpuRun(w)
-    q = torch.zeros(2, 2, 8, 128, dtype=torch.bfloat16, device="cuda")
-    out = torch.empty(2, 2, 8, 128, dtype=torch.float32, device="cuda")
-    with pytest.raises(pkv.PkvError):
-        pkv.pkv_paged_decode_attention_multi(run.desc, q, run.k_cache, run.v_cache, run.tables,
-                                             run.ctx, cfg.softmax_scale, out, run.workspace)
+    run.append()
+    gq = torch.Generator().manual_seed(7 + g)
+    q = torch.randn(4, q_len, cfg.q_heads, 128, generator=gq).to(cfg.qdt)
+    out = torch.empty(4, q_len, cfg.q_heads, 128, dtype=torch.float32, device="cuda")
+    pkv.pkv_paged_decode_attention_multi(run.desc, q.cuda(), run.k_cache, run.v_cache, run.tables,
+                                         run.ctx, cfg.softmax_scale, out, run.workspace)
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    from harness import logical_kv_fp64
+    got = out.double().cpu().numpy()
+    for b in range(4):
+        for h in range(cfg.kv_heads):
+            K, V = logical_kv_fp64(w, b, h)
+            n = K.shape[0]
+            first = max(0, q_len - n)
+            for hh in range(cfg.group):
+                hq = h * cfg.group + hh
+                ref = oracle.multi_query_decode(q[b, first:, hq].double().numpy(), K, V,
+                                                cfg.softmax_scale)
+                assert_close(got[b, first:, hq], ref, cfg, "f32", f"tok mq b{b} h{hq}")
