@@ -27,7 +27,7 @@ constexpr int kRangeMin = 32;
 constexpr int kRangeMax = 64;
 // Cost of starting a (sequence, KV head) segment, in pages, when shares are
 // cut (a state merge, an output write and a pipeline refill).
-constexpr int kSegCost = 9;
+constexpr int kSegCost = 12;
 
 // Shared-memory plan of the decode kernel (host and device agree on it).
 constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
