@@ -112,6 +112,11 @@ def test_argument_errors_return_before_any_launch():
                                         float("nan"), fake, pkv.PKV_BF16, pkv.PKV_BF16, fake,
                                         1 << 20, None)
     assert st == pkv.PKV_ERR_INVALID_ARG
+    # a batch whose per-sequence arrays do not fit the largest shared-memory plan
+    st = lib.pkv_paged_decode_attention(ctypes.byref(good), fake, fake, fake, fake, fake, 7000, 4,
+                                        0, 1.0, fake, pkv.PKV_BF16, pkv.PKV_BF16, fake, 1 << 30,
+                                        None)
+    assert st == pkv.PKV_ERR_UNSUPPORTED
 
 
 def test_argument_errors_of_the_later_entry_points():

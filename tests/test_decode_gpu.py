@@ -322,3 +322,28 @@ def test_full_size_timed_step_sampled(name):
     ref = oracle_rows(w, pairs)
     assert_close(np.stack([out[b, hq] for b, hq in pairs]), np.stack([ref[p] for p in pairs]),
                  cfg, odt, name)
+
+
+@pytest.mark.parametrize("B", [1000, 6000])
+def test_large_batches_of_short_contexts(B):
+    """Thousands of short sequences (some empty): the per-sequence arrays push
+    shared memory past two CTAs per SM (one wave becomes two) and the shares
+    hold hundreds of segments.  The timed one-kernel step, sampled rows
+    against the oracle, empty sequences exactly zero."""
+    cfg = wl.small_config(f"big_{B}", B, 32, 8, 128, "bf16", (0, 40), seed=31)
+    w = wl.generate(cfg, device="cuda")
+    run = GpuRun(w)
+    out = run.step_one_kernel("f32", overlap=True)
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    ctx = w.ctx.numpy()
+    empty = np.nonzero(ctx == 0)[0]
+    assert len(empty) > 0
+    assert torch.count_nonzero(out[torch.as_tensor(empty, device="cuda")]) == 0
+    got = out.double().cpu().numpy()
+    rng = np.random.default_rng(B)
+    bs = rng.choice(np.nonzero(ctx > 0)[0], 24, replace=False)
+    pairs = [(int(b), int(rng.integers(cfg.q_heads))) for b in bs]
+    ref = oracle_rows(w, pairs)
+    assert_close(np.stack([got[b, hq] for b, hq in pairs]), np.stack([ref[p] for p in pairs]),
+                 cfg, "f32", f"batch {B}")
