@@ -134,3 +134,32 @@ def test_prefill_unsupported_shapes():
     with pytest.raises(pkv.PkvError):
         pkv.pkv_paged_prefill_attention(run.desc, q, run.k_cache, run.v_cache, run.tables,
                                         run.ctx, starts, 2, cfg.softmax_scale, out)
+
+
+def test_prefill_full_size_sampled():
+    """The benchmarked prefill (8 sequences x 8192 tokens, each one's last 2048
+    positions the chunk) in the launch the bench times; sampled (sequence,
+    row, head) outputs against the oracle's attention row over exactly the
+    positions that row sees."""
+    cfg = wl.CONFIGS["llama3_8b_b8_ctx8192_bf16"]
+    w = wl.generate(cfg, device="cuda")
+    run = GpuRun(w)
+    run.append()
+    chunk = 2048
+    q, starts, out = _prefill(run, cfg, [chunk] * cfg.batch, "bf16", seed=5)
+    assert run.err_code() == 0
+    got = out.double().cpu().numpy()
+    rng = np.random.default_rng(8)
+    cache = {}
+    for _ in range(24):
+        b = int(rng.integers(cfg.batch))
+        j = int(rng.choice([0, 1, chunk - 1, int(rng.integers(chunk))]))
+        hq = int(rng.integers(cfg.q_heads))
+        h = hq // cfg.group
+        if (b, h) not in cache:
+            cache[(b, h)] = logical_kv_fp64(w, b, h)
+        K, V = cache[(b, h)]
+        pos = int(w.ctx[b]) - chunk + j  # this row's position: it sees 0 .. pos
+        ref = oracle.attend_row(q[int(starts[b]) + j, hq].double().numpy(), K[:pos + 1],
+                                V[:pos + 1], cfg.softmax_scale)
+        assert_close(got[int(starts[b]) + j, hq], ref, cfg, "bf16", f"b{b} row{j} h{hq}")
