@@ -146,18 +146,73 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
                :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+// The same 32-column load without its wait: r holds the columns only after
+// tmem_ld_wait(r).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+// Wait for this thread's TMEM loads.  The registers of the last load pass
+// through the wait, so no use of them can be scheduled above it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :: "memory");
+}
+// 16 consecutive 32-bit TMEM columns of this thread's lane, no wait
+__device__ __forceinline__ void tmem_st16_issue(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Packed fp32 pairs (PTX f32x2 arithmetic, sm_100 and later): one
+// instruction for two lanes' worth of add or fused multiply-add.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max of three (PTX three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+template <bool B>
+struct Masked {
+  static constexpr bool value = B;
+};
 
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
@@ -353,7 +408,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const float c2 = p.scale_log2;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
-    uint32_t r[32], sr[64];
+    uint32_t r[32];
     for (int j = 0; j < nblk; ++j) {
       const uint32_t par = (uint32_t)(j & 1);
       ok = __all_sync(0xffffffffu, wait(kBarSFull + t, par));
@@ -361,21 +416,43 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_fence_after();
       const int tok0 = j * kPfTok;
       const bool full = tok0 + kPfTok - 1 <= all_vis;  // no row masks anything here
-      // row max of the raw scores (c2 > 0 commutes with the max), in four
-      // independent chains
+      // The row's 128 scores are read in quarters of 32 columns, the next
+      // quarter's load in flight while the current one is worked on.
+      uint32_t sa[32], sb[32];
+      // row max of the raw scores (c2 > 0 commutes with the max): quarters
+      // 3, 2, 1, 0, so quarter 0 is still in sb when the P pass starts
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int th = 0; th < 2; ++th) {  // the row's 128 scores, 64 at a time
-        tmem_ld64(t_s + (uint32_t)th * 64, sr);
-        if (full) {
+      auto qmax = [&](auto mc, const uint32_t (&sq)[32], int qq) {
+        if constexpr (!decltype(mc)::value) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
+          for (int i = 0; i < 16; ++i)
+            m4[i & 3] = max3(m4[i & 3], __uint_as_float(sq[2 * i]), __uint_as_float(sq[2 * i + 1]));
         } else {
+          const int t0 = tok0 + 32 * qq;
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (tok0 + th * 64 + e <= vis) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
+          for (int i = 0; i < 16; ++i) {
+            const float a = t0 + 2 * i <= vis ? __uint_as_float(sq[2 * i]) : -INFINITY;
+            const float c = t0 + 2 * i + 1 <= vis ? __uint_as_float(sq[2 * i + 1]) : -INFINITY;
+            m4[i & 3] = max3(m4[i & 3], a, c);
+          }
         }
-      }
+      };
+      auto max_pass = [&](auto mc) {
+        tmem_ld32_issue(t_s + 96, sa);
+        tmem_ld_wait(sa);
+        tmem_ld32_issue(t_s + 64, sb);
+        qmax(mc, sa, 3);
+        tmem_ld_wait(sb);
+        tmem_ld32_issue(t_s + 32, sa);
+        qmax(mc, sb, 2);
+        tmem_ld_wait(sa);
+        tmem_ld32_issue(t_s + 0, sb);
+        qmax(mc, sa, 1);
+        tmem_ld_wait(sb);
+        qmax(mc, sb, 0);
+      };
+      if (full) max_pass(Masked<false>{});
+      else max_pass(Masked<true>{});
       const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
       // lazy rescale: keep the reference max while scores stay within 2^8 of it
       const bool grow = mx > m_ref + 8.f;
@@ -401,30 +478,60 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // P over S: per 64 tokens, the hi pairs (32 columns) then the lo pairs;
-      // the scores of a half are read before its columns are written
-#pragma unroll 1
-      for (int th = 0; th < 2; ++th) {
-        tmem_ld64(t_s + (uint32_t)th * 64, sr);
-        uint32_t hi[32], lo[32];
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+      // P over S.  Per 64 tokens the hi pairs take 32 columns, then the lo
+      // pairs 32: quarter q's pairs go to columns 64 (q / 2) + 16 (q % 2) + i
+      // (hi) and 32 more (lo).  An even quarter's lo columns hold the next
+      // quarter's scores, so that quarter is in registers before they are
+      // written.
+      const uint64_t c2x2 = f2(c2, c2), nmu2 = f2(-mu, -mu);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // four independent f32x2 chains
+      uint32_t hi[16], lo[16];
+      auto qp = [&](auto mc, const uint32_t (&sq)[32], int qq) {
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(sr[e]), c2, -mu));
-          float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), c2, -mu));
-          if (!full) {
-            const int tk = tok0 + th * 64 + e;
+        for (int i = 0; i < 16; ++i) {
+          const float2 y = f2_split(fma2(f2(__uint_as_float(sq[2 * i]),
+                                            __uint_as_float(sq[2 * i + 1])), c2x2, nmu2));
+          float p0 = ex2(y.x), p1 = ex2(y.y);
+          if constexpr (decltype(mc)::value) {
+            const int tk = tok0 + 32 * qq + 2 * i;
             if (tk > vis) p0 = 0.f;
             if (tk + 1 > vis) p1 = 0.f;
           }
-          l4[(e >> 1) & 3] += p0 + p1;
-          hi[e / 2] = pack2<BF16>(p0, p1);
-          const float2 f = unpack2<BF16>(hi[e / 2]);
-          lo[e / 2] = pack2<BF16>(p0 - f.x, p1 - f.y);
+          const uint64_t pp = f2(p0, p1);
+          acc[i & 3] = add2(acc[i & 3], pp);
+          hi[i] = pack2<BF16>(p0, p1);
+          const float2 hf = unpack2<BF16>(hi[i]);
+          const float2 l = f2_split(sub2(pp, f2(hf.x, hf.y)));
+          lo[i] = pack2<BF16>(l.x, l.y);
         }
-        l_sum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-        tmem_st32(t_s + (uint32_t)th * 64, hi);
-        tmem_st32(t_s + (uint32_t)th * 64 + 32, lo);
+      };
+      auto qst = [&](int qq) {
+        const uint32_t c = (uint32_t)(64 * (qq >> 1) + 16 * (qq & 1));
+        tmem_st16_issue(t_s + c, hi);
+        tmem_st16_issue(t_s + c + 32, lo);
+      };
+      auto p_pass = [&](auto mc) {
+        tmem_ld32_issue(t_s + 32, sa);
+        qp(mc, sb, 0);
+        tmem_ld_wait(sa);
+        qst(0);
+        tmem_ld32_issue(t_s + 64, sb);
+        qp(mc, sa, 1);
+        tmem_ld_wait(sb);
+        qst(1);
+        tmem_ld32_issue(t_s + 96, sa);
+        qp(mc, sb, 2);
+        tmem_ld_wait(sa);
+        qst(2);
+        qp(mc, sa, 3);
+        qst(3);
+      };
+      if (full) p_pass(Masked<false>{});
+      else p_pass(Masked<true>{});
+      tmem_st_wait();
+      {
+        const float2 a0 = f2_split(add2(acc[0], acc[1])), a1 = f2_split(add2(acc[2], acc[3]));
+        l_sum += (a0.x + a0.y) + (a1.x + a1.y);
       }
       // rows of V past the context hold whatever the pool or an older block
       // left: tile 0 zeroes them before it hands over (the MMA multiplies them
