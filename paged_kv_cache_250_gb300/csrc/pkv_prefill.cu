@@ -285,6 +285,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == 9) {
     // ---------------------------------------------------------- copies
+    // Lane 0 arms the barriers; lane i < 8 reads the block-table entry of
+    // page i of a block (one block ahead, so the lookups' latency hides under
+    // the previous block's waits) and issues that page's copies, for K and
+    // for V from the same entry.
     if (lane == 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
@@ -295,31 +299,45 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int c = 0; c < NH; ++c)
           tma_load_3d(base + kOffQ + (uint32_t)(t * NH + c) * kQHalf, &tmq, bar(kBarQ), c * 64,
                       h * G, q0 + tok_base + t * tpt);
-      for (int j = 0; j < nblk; ++j) {
-        const int bb = j & 1;
-        const int pg0 = j * kPfPages;
-        const int npg = min(kPfPages, np - pg0);
-        for (int v = 0; v < 2; ++v) {  // K, then V of block j
-          const int full = (v ? kBarVFull : kBarKFull) + bb;
-          if (j >= 2 && !wait((v ? kBarVFree : kBarKFree) + bb, (uint32_t)(((j - 2) >> 1) & 1)))
-            break;
+    }
+    const int64_t trow = (int64_t)b * p.MBS;
+    auto table_entry = [&](int j) -> int {
+      const int pg = j * kPfPages + lane;
+      return lane < kPfPages && pg < np ? p.block_tables[trow + pg] : 0;
+    };
+    int cur = table_entry(0);
+    for (int j = 0; j < nblk; ++j) {
+      const int bb = j & 1;
+      const int npg = min(kPfPages, np - j * kPfPages);
+      const int nxt = j + 1 < nblk ? table_entry(j + 1) : 0;
+      int blk = cur;
+      if (lane < npg && (blk < 0 || blk >= p.NB)) {  // the copy reads the fill value (zeros) past the pool
+        report_error(p.err_word, PKV_ERR_BOUNDS);
+        blk = p.NB;
+      }
+      bool ok = true;
+      for (int v = 0; v < 2; ++v) {  // K, then V of block j
+        const int full = (v ? kBarVFull : kBarKFull) + bb;
+        if (j >= 2)
+          ok = __all_sync(0xffffffffu, wait((v ? kBarVFree : kBarKFree) + bb,
+                                            (uint32_t)(((j - 2) >> 1) & 1)));
+        if (!ok) break;
+        if (lane == 0) {
           armed[full] = armed[full] + 1;
           mbar_arrive_expect_tx(bar(full), (uint32_t)npg * NH * kPageSize * 128);
-          const uint32_t dst = base + (v ? kOffV : kOffK) + (uint32_t)bb * NH * kKHalf;
-          for (int i = 0; i < npg; ++i) {
-            int blk = p.block_tables[(int64_t)b * p.MBS + pg0 + i];
-            if (blk < 0 || blk >= p.NB) {  // the copy reads the fill value (zeros) past the pool
-              report_error(p.err_word, PKV_ERR_BOUNDS);
-              blk = p.NB;
-            }
-            const int r = (blk * p.Hkv + h) * kPageSize;
-            for (int c = 0; c < NH; ++c)
-              tma_load_2d_plain(dst + (uint32_t)c * kKHalf + (uint32_t)i * kPageSize * 128,
-                                v ? (const void*)&tmv : (const void*)&tmk, bar(full), c * 64, r);
-          }
         }
-        if (*abort_flag) break;
+        __syncwarp();
+        if (lane < npg) {
+          const uint32_t dst = base + (v ? kOffV : kOffK) + (uint32_t)bb * NH * kKHalf +
+                               (uint32_t)lane * kPageSize * 128;
+          const int r = (blk * p.Hkv + h) * kPageSize;
+          for (int c = 0; c < NH; ++c)
+            tma_load_2d_plain(dst + (uint32_t)c * kKHalf,
+                              v ? (const void*)&tmv : (const void*)&tmk, bar(full), c * 64, r);
+        }
       }
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+      cur = nxt;
     }
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMAs
