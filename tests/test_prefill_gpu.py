@@ -163,3 +163,43 @@ def test_prefill_full_size_sampled():
         ref = oracle.attend_row(q[int(starts[b]) + j, hq].double().numpy(), K[:pos + 1],
                                 V[:pos + 1], cfg.softmax_scale)
         assert_close(got[int(starts[b]) + j, hq], ref, cfg, "bf16", f"b{b} row{j} h{hq}")
+
+
+def test_prefill_empty_chunks_skip_their_sequences():
+    """Sequences with no new rows in the batch take no work and write nothing;
+    the others match the oracle."""
+    cfg, w, run = _setup("empty", 8, 2, "bf16", [100, 300, 50, 700], 66)
+    chunks = [0, 130, 0, 5]
+    q, starts, out = _prefill(run, cfg, chunks, "f32", seed=2)
+    assert run.err_code() == 0
+    ref = _expected(w, cfg, q, starts, chunks)
+    got = out.double().cpu().numpy()
+    assert set(b for b, _ in ref) == {1, 3}
+    for (b, hq), r in ref.items():
+        s0 = int(starts[b])
+        assert_close(got[s0:s0 + chunks[b], hq], r, cfg, "f32", f"empty b{b} h{hq}")
+
+
+@pytest.mark.parametrize("bad", [-1, "pool"])
+def test_prefill_bad_table_entry_is_reported_not_read(bad):
+    """A table entry outside the pool in a page the chunk sees: the error word
+    says so, the copy reads the fill value instead, outputs stay finite."""
+    cfg, w, run = _setup("badtab", 8, 2, "bf16", [300, 600], 67)
+    tables = run.tables.clone()
+    tables[1, 5] = -1 if bad == -1 else w.num_blocks  # page 5 of sequence 1 (positions 80..95)
+    chunks = [20, 200]
+    g = torch.Generator().manual_seed(303)
+    q = torch.randn(sum(chunks), cfg.q_heads, cfg.head_dim, generator=g).to(cfg.qdt).cuda()
+    starts = torch.tensor([0, 20, 220], dtype=torch.int32, device="cuda")
+    out = torch.full((220, cfg.q_heads, cfg.head_dim), float("nan"), dtype=torch.float32,
+                     device="cuda")
+    pkv.pkv_paged_prefill_attention(run.desc, q, run.k_cache, run.v_cache, tables, run.ctx,
+                                    starts, 200, cfg.softmax_scale, out)
+    torch.cuda.synchronize()
+    assert run.err_code() == pkv.PKV_ERR_BOUNDS
+    assert torch.all(torch.isfinite(out))
+    # sequence 0 does not touch the bad entry: its rows still match the oracle
+    ref = _expected(w, cfg, q.cpu(), starts.cpu(), [20, 0])
+    got = out.double().cpu().numpy()
+    for (b, hq), r in ref.items():
+        assert_close(got[0:20, hq], r, cfg, "f32", f"badtab h{hq}")
