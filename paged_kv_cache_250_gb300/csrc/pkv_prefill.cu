@@ -15,13 +15,18 @@
 //                   t, TMEM lane t, so the online softmax (running max m, sum
 //                   l, rescale of O) needs no shuffles;
 //   warp 8          issues the MMAs (one thread);
-//   warp 9          issues the tensor copies (one thread).
+//   warp 9          the tensor copies: lane 0 arms the barriers, lanes 0-7
+//                   read a block's eight table entries one block ahead and
+//                   issue one page's copies each.
 // Per block of 128 cached tokens (8 pages), for each tile:
 //   S = Q K^T    tcgen05.mma, M 128 x N 128 x K 128 (d), both operands K-major
 //                128-byte-swizzled tiles as the tensor copies write them, the
 //                scores landing in tensor memory;
-//   softmax      tcgen05.ld of the row, mask, exp2, P as a bf16 (or fp16)
-//                hi + lo pair written back over the row's scores (tcgen05.st);
+//   softmax      the row read from tensor memory 32 columns at a time (the
+//                next load in flight under the current quarter's work), its
+//                max, then exp2 and P as a bf16 (or fp16) hi + lo pair written
+//                back over the row's scores (tcgen05.st); blocks that every
+//                row sees whole skip the masking code;
 //   O += P V     tcgen05.mma with A read from tensor memory, twice (hi and lo)
 //                per 64 tokens, M 128 x N 128 (d) x K 16 per instruction; V is
 //                used where the copies put it, as an MN-major operand.
