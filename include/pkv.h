@@ -259,9 +259,11 @@ PKV_API pkv_status pkv_decode_step(
  *   scale         > 0 (the softmax scale); otherwise PKV_ERR_INVALID_ARG.
  *   out           [total_q][num_q_heads][head_dim] of out_dtype (F16 | BF16 |
  *                 F32).
- * A sequence whose rows, length or table break these rules is a device-
- * detected PKV_ERR_BOUNDS; its output rows are then not written.  No
- * workspace.  Inputs are read after the preceding kernel on the stream
+ * A sequence whose row count or length breaks these rules is a device-
+ * detected PKV_ERR_BOUNDS and its output rows are not written.  A table
+ * entry outside [0, num_blocks) in a page the chunk sees is PKV_ERR_BOUNDS
+ * too: that page is read as zeros, never from outside the pool, and the
+ * sequence's rows are written but meaningless.  No workspace.  Inputs are read after the preceding kernel on the stream
  * completes (the kernel is launched as a programmatic dependent).  Results
  * are deterministic: each output row is one CTA's fixed sequence of MMAs. */
 PKV_API pkv_status pkv_paged_prefill_attention(
