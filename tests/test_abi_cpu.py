@@ -177,3 +177,26 @@ def test_argument_errors_of_the_later_entry_points():
     st = lib.pkv_kv_append(ctypes.byref(tok64), fake, fake, fake, fake, fake, 1, pkv.PKV_BF16,
                            None)
     assert st == pkv.PKV_ERR_UNSUPPORTED
+
+
+def test_prefill_argument_errors():
+    """The prefill's host checks, each before any CUDA call: the scale must be
+    positive (the kernel takes row maxima of the raw scores), the output a
+    16- or 32-bit float, the pointers present and aligned, the table width
+    positive."""
+    lib = pkv.load_library()
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)  # not 16-byte aligned
+    good = pkv.make_desc(64, 16, 2, 8, 128, pkv.PKV_BF16)
+
+    def call(q=fake, q_start=fake, scale=1.0, out_dtype=pkv.PKV_F32, mbs=4, out=fake):
+        return lib.pkv_paged_prefill_attention(ctypes.byref(good), q, fake, fake, fake, fake,
+                                               q_start, 2, 8, 4, mbs, scale, out, pkv.PKV_BF16,
+                                               out_dtype, None)
+    for scale in (0.0, -0.5, float("nan")):
+        assert call(scale=scale) == pkv.PKV_ERR_INVALID_ARG
+    assert call(out_dtype=pkv.PKV_FP8_E4M3) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(q=odd) == pkv.PKV_ERR_INVALID_ARG
+    assert call(out=odd) == pkv.PKV_ERR_INVALID_ARG
+    assert call(q_start=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(mbs=0) == pkv.PKV_ERR_INVALID_ARG
