@@ -47,3 +47,25 @@ def test_a_query_never_sees_later_tokens():
     moved = oracle.multi_query_decode(Q, K2, V2, 0.3)
     assert np.array_equal(moved[:-1], base[:-1])
     assert not np.allclose(moved[-1], base[-1])
+
+
+def test_prefill_chunk_rows_match_library_sdpa():
+    """The prefill reading of the same function (a long chunk of new rows at
+    the end of a longer context, each row seeing positions 0 .. itself)
+    against PyTorch's scaled_dot_product_attention with that mask, in fp64;
+    both whole prompts (chunk = context) and chunks after a cached prefix."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(14)
+    for n, QL, d in [(300, 120, 64), (257, 257, 32), (64, 1, 128), (513, 40, 16)]:
+        Q = rng.standard_normal((QL, d))
+        K = rng.standard_normal((n, d))
+        V = rng.standard_normal((n, d))
+        scale = d ** -0.5
+        pos = torch.arange(n - QL, n)[:, None]
+        mask = torch.arange(n)[None, :] <= pos  # True: attend
+        ref = F.scaled_dot_product_attention(torch.from_numpy(Q)[None], torch.from_numpy(K)[None],
+                                             torch.from_numpy(V)[None], attn_mask=mask[None],
+                                             scale=scale)[0].numpy()
+        got = oracle.multi_query_decode(Q, K, V, scale)
+        assert np.allclose(got, ref, rtol=0, atol=1e-12), (n, QL, d)
