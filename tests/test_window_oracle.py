@@ -41,3 +41,22 @@ def test_special_cases():
     # a window of one and no sinks: each query sees only itself
     one = oracle.window_decode(Q, K, V, 0.3, 1, 0)
     assert np.array_equal(one, V[n - 3:])
+
+
+def test_matches_library_sdpa_with_the_window_mask():
+    """Against PyTorch's scaled_dot_product_attention in fp64 with the
+    boolean mask built from positions (no numpy softmax involved)."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(23)
+    for n, QL, w, s in [(200, 1, 64, 4), (200, 8, 17, 16), (90, 3, 1, 0), (130, 2, 500, 3)]:
+        Q, K, V = (rng.standard_normal((QL, 32)), rng.standard_normal((n, 32)),
+                   rng.standard_normal((n, 32)))
+        t = torch.arange(n)[None, :]
+        p = torch.arange(n - QL, n)[:, None]
+        mask = (t <= p) & ((t >= p - w + 1) | (t < s))
+        ref = F.scaled_dot_product_attention(torch.from_numpy(Q)[None], torch.from_numpy(K)[None],
+                                             torch.from_numpy(V)[None], attn_mask=mask[None],
+                                             scale=0.2)[0].numpy()
+        got = oracle.window_decode(Q, K, V, 0.2, w, s)
+        assert np.allclose(got, ref, rtol=0, atol=1e-12), (n, QL, w, s)
