@@ -34,7 +34,7 @@ def _rank(rank: int, world: int, port: int, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of this threaded process
     mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == pytest.approx(3.5)
 
