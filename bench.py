@@ -563,7 +563,7 @@ def run_reference(args, cfg):
 # ---------------------------------------------------------------- block copy
 def run_copy_blocks(args, device):
     """pkv_copy_blocks alone: copy-on-write of whole blocks (8192 bf16 blocks of
-    8 KV heads x 16 tokens x 128, K and V: 1.07 GB read + 1.07 GB written per
+    8 KV heads x 16 tokens x 128, K and V: 0.54 GB read + 0.54 GB written per
     step, far above L2), K steps in one CUDA graph, CUDA events around it."""
     NB, Hkv, d, n = 16384, 8, 128, 8192
     g = torch.Generator().manual_seed(7)
@@ -601,6 +601,8 @@ def run_copy_blocks(args, device):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) blocks)",
             "config": {"workload": f"copy_blocks_{n}x_bf16_h{Hkv}_d{d}", "blocks": n,
                        "block_bytes_per_cache": Hkv * wl.PAGE * d * 2,
+                       "l2": f"{2 * n * Hkv * wl.PAGE * d * 2 / 1e9:.2f} GB read and as much "
+                             "written per call, far above L2",
                        "timing": "K copies in one CUDA graph, CUDA events on the stream"},
             "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
@@ -688,6 +690,8 @@ def run_multi_query(args, cfg, device, windowed: bool = False):
             "data": "synthetic (seeded N(0,1) q/k/v, the workload's lengths and tables)",
             "config": {**workload_config(cfg, st.w.ctx), **extra,
                        "tokens_per_s_per_layer": round(cfg.batch * qlen / (ms * 1e-3), 1),
+                       "l2": f"rotating {R} cache-pool copies ({R * pool_bytes / 1e6:.0f} MB, "
+                             ">= 4x L2 where the pool allows); every call reads cold pages",
                        "timing": "K calls in one CUDA graph, CUDA events on the stream"},
             "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
@@ -752,6 +756,7 @@ def run_prefill(args, cfg, device):
     if int(st.err.item()) != 0:
         raise RuntimeError("device error word set")
     ms = e0.elapsed_time(e1) / K
+    pool_mb = st.kc[0].numel() * st.kc[0].element_size() * 2 / 1e6
     flops = prefill_flops(st.w.ctx, args.chunk, cfg.q_heads, cfg.head_dim)
     tflops = flops / (ms * 1e-3) / 1e12
     peak = measured_tensor_peak()
@@ -763,6 +768,8 @@ def run_prefill(args, cfg, device):
             "data": "synthetic (seeded N(0,1) q/k/v, the workload's lengths and tables)",
             "config": {**workload_config(cfg, st.w.ctx), "chunk": args.chunk,
                        "query_rows": total, "flops_per_call": flops,
+                       "l2": f"one cache pool ({pool_mb:.0f} MB of K and V, above L2) read "
+                             "by every call",
                        "timing": "K calls in one CUDA graph, CUDA events on the stream"},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak[0],
                          "unit": "TFLOP/s", "frac": round(tflops / peak[0], 4),
