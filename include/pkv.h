@@ -147,7 +147,12 @@ PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t ba
  * gathers K and V); [DF] running-summary paragraph.
  *   q             [batch][num_q_heads][head_dim] of q_dtype (F16 | BF16;
  *                 for 16-bit caches equal to cache_dtype).  With an FP8
- *                 cache q is used in fp16 and must lie within +-65504.
+ *                 cache the kernel meets q on the fp16 MMA: a bf16 q is
+ *                 first scaled, per query head, by a power of two that
+ *                 brings its largest element into [2^14, 2^15), and the
+ *                 score scale undoes it, so any finite bf16 q is taken
+ *                 whole (elements more than 2^28 below their head's largest
+ *                 keep fewer bits).
  *   block_tables  int32 [batch][max_blocks_per_seq]; entry p of row b is the
  *                 block holding tokens p*P .. p*P+P-1 of sequence b.  Rows
  *                 may share blocks (prefix sharing); entries past a
@@ -323,10 +328,14 @@ PKV_API pkv_status pkv_decode_step_fused(
  * nothing.
  *   - Shapes whose workspace (pkv_decode_workspace_bytes) exceeds
  *     PKV_NOALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE; other argument
- *     errors are those of pkv_paged_decode_attention.
+ *     errors are those of pkv_paged_decode_attention.  Every argument is
+ *     checked before anything is put on the stream.
  *   - The first call on each device looks up the scratch array's device
- *     address (cudaGetSymbolAddress); make that first call before any stream
- *     capture on that device.
+ *     address (cudaGetSymbolAddress) and keeps it for the life of the
+ *     process; make that first call before any stream capture on that
+ *     device.  The kept address belongs to the device's primary context (the
+ *     one the CUDA runtime uses): calls from another context on the device,
+ *     or after a cudaDeviceReset, are not supported.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; each call first clears, on `stream`, the part that must start
  *     at zero.  Calls whose executions overlap on the GPU (other streams,

@@ -219,6 +219,23 @@ pkv_status decode_checks(const pkv_cache_desc* desc, const void* q, const void* 
   return PKV_OK;
 }
 
+}  // namespace
+
+namespace pkv {
+pkv_status decode_validate(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
+                           int32_t max_context_len_hint, float scale, const void* out,
+                           pkv_dtype q_dtype, pkv_dtype out_dtype, const void* workspace,
+                           size_t workspace_bytes) {
+  return decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
+                       max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
+                       workspace, workspace_bytes);
+}
+}  // namespace pkv
+
+namespace {
+
 pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_cache,
                        const void* v_cache, const int32_t* block_tables,
                        const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,

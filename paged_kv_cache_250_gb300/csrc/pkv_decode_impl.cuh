@@ -462,7 +462,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   uint32_t qf[C::kKSteps][2];
   float o[kMT][4];
   float m2[2], l2[2];
-  float c2 = 0.f;  // score scale in log2 units (E4M3: times the K scale)
+  // score scale in log2 units (E4M3: times the K scale) for the lane's two
+  // C-fragment columns 2 c4 and 2 c4 + 1
+  float c2a = 0.f, c2b = 0.f;
 
   auto reset_state = [&]() {
 #pragma unroll
@@ -497,22 +499,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         qf[ks][1] = b1;
       }
     } else {
+      // FP8 pages meet q on the fp16 MMA.  A bf16 q can lie outside fp16's
+      // range, so each column is brought to [2^14, 2^15) by a power of two
+      // (exact), which the column's score scale undoes (also exact).
+      uint2 raw[C::kKSteps];
+      float amax = 0.f;
 #pragma unroll
       for (int ks = 0; ks < C::kKSteps; ++ks) {
-        uint32_t b0 = 0, b1 = 0;
-        if (real) {
-          const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c4);
-          const float2 f01 = unpack2<QBF16>(raw4.x);
-          const float2 f23 = unpack2<QBF16>(raw4.y);
-          b0 = pack2<false>(f01.x, f01.y);
-          b1 = pack2<false>(f23.x, f23.y);
+        raw[ks] = make_uint2(0u, 0u);
+        if (real) raw[ks] = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c4);
+        if constexpr (QBF16) {
+          const float2 f01 = unpack2<true>(raw[ks].x), f23 = unpack2<true>(raw[ks].y);
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)),
+                                   fmaxf(fabsf(f23.x), fabsf(f23.y))));
         }
-        qf[ks][0] = b0;
-        qf[ks][1] = b1;
       }
+      int e = 0;  // column scale 2^e
+      if constexpr (QBF16) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (amax > 0.f) e = min(112, max(-112, ((__float_as_int(amax) >> 23) & 0xff) - 127 - 14));
+      }
+      const float down = __int_as_float((127 - e) << 23);
+#pragma unroll
+      for (int ks = 0; ks < C::kKSteps; ++ks) {
+        const float2 f01 = unpack2<QBF16>(raw[ks].x);
+        const float2 f23 = unpack2<QBF16>(raw[ks].y);
+        qf[ks][0] = pack2<false>(f01.x * down, f01.y * down);
+        qf[ks][1] = pack2<false>(f23.x * down, f23.y * down);
+      }
+      // the lane's C-fragment columns 2 c4, 2 c4 + 1 are B-fragment columns
+      // of lanes 8 c4 and 8 c4 + 4
+      const int ea = __shfl_sync(0xffffffffu, e, 8 * c4);
+      const int eb = __shfl_sync(0xffffffffu, e, 8 * c4 + 4);
+      float c2 = p.scale_log2;
+      if constexpr (CACHE == kCacheE4M3) c2 *= p.k_scale[h];
+      c2a = c2 * __int_as_float((127 + ea) << 23);
+      c2b = c2 * __int_as_float((127 + eb) << 23);
+      return;
     }
-    c2 = p.scale_log2;
-    if constexpr (CACHE == kCacheE4M3) c2 *= p.k_scale[h];
+    c2a = c2b = p.scale_log2;
   };
 
   // ---- S^T[16 tok][8] = K . Q^T for one page, on two accumulator chains
@@ -625,7 +651,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       const int v = valids[i];
       const int rem = v & kRemMask;  // tokens from the page's start to the context's end
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[i][e] *= c2;
+      for (int e = 0; e < 4; ++e) x[i][e] *= (e & 1) ? c2b : c2a;
       if constexpr (kTok) {
         x[i][0] *= ksc[i][0];  // rows past the context are masked below
         x[i][1] *= ksc[i][0];

@@ -129,6 +129,13 @@ cudaError_t launch_decode_multi_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_e4m3(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_e4m3_tok(const DecodeLaunch& l);
+// The argument checks of pkv_paged_decode_attention, with nothing launched.
+pkv_status decode_validate(const pkv_cache_desc* desc, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
+                           int32_t max_context_len_hint, float scale, const void* out,
+                           pkv_dtype q_dtype, pkv_dtype out_dtype, const void* workspace,
+                           size_t workspace_bytes);
 // Clears, on the stream, the parts of a decode workspace that must be zero
 // when a call begins (whatever an earlier, failed call left there).
 cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,

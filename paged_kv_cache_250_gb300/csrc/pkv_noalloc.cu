@@ -65,6 +65,12 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(
   if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
+  // every argument is checked before anything is put on the stream
+  const pkv_status st = pkv::decode_validate(
+      desc, q, k_cache, v_cache, block_tables, context_lens, batch, max_blocks_per_seq,
+      max_context_len_hint, scale, out, q_dtype, out_dtype, scratch,
+      (size_t)PKV_NOALLOC_SCRATCH_BYTES);
+  if (st != PKV_OK) return st;
   // the arrival counters must start at zero whatever an earlier call left
   if (pkv::decode_workspace_clear(scratch, (size_t)PKV_NOALLOC_SCRATCH_BYTES, desc, batch,
                                   max_blocks_per_seq, max_context_len_hint,

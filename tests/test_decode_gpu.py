@@ -75,6 +75,29 @@ def test_ragged_sweep_fp8(g, q_dtype):
     assert_close(out_bf, ref, cfg, "bf16", "fp8 bf16 out")
 
 
+@pytest.mark.parametrize("cache", ["e4m3", "e4m3tok"])
+@pytest.mark.parametrize("mag", [1e5, 1e-30])
+def test_fp8_bf16_q_outside_fp16_range(cache, mag):
+    # A bf16 q far outside fp16's range (|q| up to ~4e5, or down to ~1e-31)
+    # against an FP8 cache: the kernel meets q on the fp16 MMA after a
+    # per-head power-of-two scale, so the result must match the oracle, never
+    # an inf or a flushed row.  The softmax scale carries 1/mag so that the
+    # attention pattern is that of an ordinary q.
+    import dataclasses
+    cfg = wl.small_config(f"qrange_{cache}", len(RAGGED), 8, 2, 128, cache, 1, seed=29)
+    cfg = dataclasses.replace(cfg, scale=1.0 / (mag * np.sqrt(128.0)))
+    w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
+    w.q = (w.q.float() * mag).to(torch.bfloat16)  # the oracle reads the same bf16 q
+    assert float(w.q.float().abs().max()) > 65504.0 or float(w.q.float().abs().max()) < 6e-5
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    ref = oracle_all(w)
+    err = assert_close(out, ref, cfg, "f32", f"fp8 q x {mag}")
+    assert err < 2e-3
+
+
 def test_many_splits_long_sequence():
     # one long sequence spread over every warp of the grid, plus short ones
     cfg = wl.small_config("long", 3, 8, 2, 128, "bf16", 1, seed=5)

@@ -60,3 +60,31 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_paged_decode_attention_noalloc(desc, q, kc, vc, tables, ctx, 0.1, out)
     assert e.value.status == pkv.PKV_ERR_WORKSPACE
+
+
+def test_noalloc_on_a_side_stream_and_argument_errors_first():
+    # Each call clears its arrival counters on the stream it is given: two
+    # calls in a row on a non-default stream must match the regular entry
+    # point.  An invalid argument is refused before anything is queued.
+    cfg = wl.small_config("noalloc_stream", 5, 8, 2, 128, "bf16", 1, seed=22)
+    w = wl.generate(cfg, ctx_override=torch.tensor([3, 700, 40, 1, 2048]))
+    run = GpuRun(w)
+    run.append()
+    ref = run.decode("f32")
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    outs = [torch.full_like(ref, float("nan")) for _ in range(2)]
+    with torch.cuda.stream(side):
+        for out in outs:
+            pkv.pkv_paged_decode_attention_noalloc(run.desc, run.q, run.k_cache, run.v_cache,
+                                                   run.tables, run.ctx, cfg.softmax_scale, out,
+                                                   stream=side)
+    side.synchronize()
+    assert run.err_code() == 0
+    for out in outs:
+        assert np.abs(out.double().cpu().numpy() - ref.double().cpu().numpy()).max() <= 2e-3
+    bad = torch.empty_like(ref)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_paged_decode_attention_noalloc(run.desc, run.q, run.k_cache, run.v_cache,
+                                               run.tables, run.ctx, float("nan"), bad)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
