@@ -632,13 +632,17 @@ def run_multi_query(args, cfg, device, windowed: bool = False):
     decode plus the extra q and output rows, counting under a window only the
     positions some token sees."""
     qlen = args.qlen
-    if cfg.group * qlen > 8:
-        raise SystemExit(f"q_len {qlen} x group {cfg.group} exceeds the 8 MMA columns")
+    if not 1 <= qlen <= 8:
+        raise SystemExit(f"q_len {qlen}: 1 to 8 query tokens per sequence are built")
     hint = {"llama3_8b_b32_ctx1-4096_bf16": 4096}.get(cfg.name, 0)
     st = Step(cfg, device, 1, hint)
     pool_bytes = st.kc[0].numel() * st.kc[0].element_size() * 2
     R = max(1, min(8, -(-4 * L2_BYTES // pool_bytes)))
     st = Step(cfg, device, R, hint)
+    # partials of group x q_len columns
+    n = pkv.pkv_decode_workspace_bytes_multi(st.desc, cfg.batch, qlen, st.w.max_blocks_per_seq,
+                                             hint)
+    st.ws = torch.zeros(n, dtype=torch.uint8, device=device)
     g = torch.Generator().manual_seed(cfg.seed + 77)
     q = torch.randn(cfg.batch, qlen, cfg.q_heads, cfg.head_dim, generator=g).to(cfg.qdt).to(device)
     out = torch.empty(cfg.batch, qlen, cfg.q_heads, cfg.head_dim, dtype=st.out.dtype, device=device)
@@ -695,7 +699,10 @@ def run_multi_query(args, cfg, device, windowed: bool = False):
                        "timing": "K calls in one CUDA graph, CUDA events on the stream"},
             "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
-                         "kernel": f"decode_kernel (q_len {qlen}{', window' if windowed else ''})",
+                         "kernel": (f"decode_kernel (q_len 1{', window' if windowed else ''})"
+                                    if qlen == 1 else
+                                    f"mq::decode_kernel (q_len {qlen}, {cfg.group * qlen} "
+                                    f"(token, head) columns{', window' if windowed else ''})"),
                          "peak_kind": peak_kind},
             "gpu_launches": K}
 

@@ -135,10 +135,20 @@ PKV_API pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache,
  * with the same descriptor and a batch of at most B (any max_blocks_per_seq
  * and hint); pass its full size.  After a call that reported
  * PKV_ERR_TIMEOUT, zero it again.  Calls that share a workspace must not
- * overlap. */
+ * overlap.  It serves the multi-query and windowed calls for
+ * (num_q_heads / num_kv_heads) * q_len <= 8. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t max_blocks_per_seq,
                                   int32_t max_context_len_hint);
+
+/* The same for the multi-query and windowed calls with up to q_len (1 .. 8)
+ * query tokens per sequence: their split partials hold group * q_len
+ * columns (rounded up to a power of two).  A workspace sized for (B, Q)
+ * serves every call with the same descriptor, a batch of at most B and at
+ * most Q query tokens.  Returns 0 on invalid arguments or without a device. */
+PKV_API size_t pkv_decode_workspace_bytes_multi(const pkv_cache_desc* desc, int32_t batch,
+                                        int32_t q_len, int32_t max_blocks_per_seq,
+                                        int32_t max_context_len_hint);
 
 /* Decode attention for one layer.
  * [KVFA] KV-cache section ((1,N) row per step), Flash Attention and
@@ -193,9 +203,19 @@ PKV_API pkv_status pkv_paged_decode_attention(
  * batch * q_len rows), and context_lens counts them.  A token that sees no
  * position (context_lens[b] < q_len) gets a zero row.
  *   q, out        [batch][q_len][num_q_heads][head_dim].
- *   q_len         1 .. 8 / (num_q_heads / num_kv_heads); larger returns
+ *   q_len         1 .. 8 at any group size; larger returns
  *                 PKV_ERR_UNSUPPORTED.  q_len 1 is pkv_paged_decode_attention.
- * The workspace of pkv_decode_workspace_bytes serves any supported q_len.
+ *                 Up to 8 (query token, head) pairs of a KV head share one
+ *                 tensor-core column block; 16 take two per warp, and 32 or
+ *                 64 split every page's columns over 2 or 4 warps, so each
+ *                 page is still read from memory once.
+ *   workspace     of at least pkv_decode_workspace_bytes_multi(q_len) bytes
+ *                 (pkv_decode_workspace_bytes suffices while
+ *                 (num_q_heads / num_kv_heads) * q_len <= 8).
+ * For q_len > 1 each CTA's pages go to whichever of its warps is free first,
+ * so repeated calls can differ by the order in which fp32 partial sums are
+ * added (a few units in the last place of an fp32 output); q_len 1 is
+ * bitwise repeatable.
  * Other arguments and guarantees as for pkv_paged_decode_attention. */
 PKV_API pkv_status pkv_paged_decode_attention_multi(
     const pkv_cache_desc* desc, const void* q, const void* k_cache,

@@ -6,6 +6,8 @@ memory and streams.  The functions carry the C names:
 
     pkv_kv_append                 write new K/V rows into their cache slots
     pkv_decode_workspace_bytes    workspace size for a decode call
+    pkv_decode_workspace_bytes_multi  the same for q_len query tokens per
+                                  sequence (multi-query and windowed calls)
     pkv_paged_decode_attention    one (1,N) attention row per query head
     pkv_paged_decode_attention_multi  q_len new tokens per sequence, causal
     pkv_paged_decode_attention_window  the same under a sliding window with
@@ -42,6 +44,7 @@ __all__ = [
     "pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "PKV_NOALLOC_SCRATCH_BYTES", "pkv_copy_blocks",
+    "pkv_decode_workspace_bytes_multi",
     "pkv_paged_decode_attention_multi", "pkv_paged_decode_attention_window",
     "pkv_decode_step_fused", "pkv_paged_prefill_attention",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE",
@@ -60,6 +63,7 @@ EXPORTED_SYMBOLS = (
     "pkv_decode_step", "pkv_kv_bytes_per_token", "pkv_status_string", "pkv_version",
     "pkv_paged_decode_attention_noalloc", "pkv_copy_blocks", "pkv_paged_decode_attention_multi",
     "pkv_paged_decode_attention_window", "pkv_decode_step_fused", "pkv_paged_prefill_attention",
+    "pkv_decode_workspace_bytes_multi",
 )
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -113,6 +117,8 @@ def load_library():
         lib.pkv_kv_append.argtypes = [D, P, P, P, P, P, I32, I32, P]
         lib.pkv_decode_workspace_bytes.restype = SZ
         lib.pkv_decode_workspace_bytes.argtypes = [D, I32, I32, I32]
+        lib.pkv_decode_workspace_bytes_multi.restype = SZ
+        lib.pkv_decode_workspace_bytes_multi.argtypes = [D, I32, I32, I32, I32]
         lib.pkv_paged_decode_attention.restype = I32
         lib.pkv_paged_decode_attention.argtypes = [D, P, P, P, P, P, I32, I32, I32,
                                                    ctypes.c_float, P, I32, I32, P, SZ, P]
@@ -230,6 +236,15 @@ def pkv_decode_workspace_bytes(desc: CacheDesc, batch: int, max_blocks_per_seq: 
     return int(lib.pkv_decode_workspace_bytes(ctypes.byref(desc), int(batch),
                                               int(max_blocks_per_seq),
                                               int(max_context_len_hint)))
+
+
+def pkv_decode_workspace_bytes_multi(desc: CacheDesc, batch: int, q_len: int,
+                                     max_blocks_per_seq: int,
+                                     max_context_len_hint: int = 0) -> int:
+    lib = load_library()
+    return int(lib.pkv_decode_workspace_bytes_multi(ctypes.byref(desc), int(batch), int(q_len),
+                                                    int(max_blocks_per_seq),
+                                                    int(max_context_len_hint)))
 
 
 def pkv_paged_decode_attention(desc: CacheDesc, q: torch.Tensor, k_cache: torch.Tensor,

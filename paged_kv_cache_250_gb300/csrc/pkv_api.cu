@@ -99,17 +99,22 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace: from the front, the split partials (one slot per CTA of the
 // largest grid plus one per segment, slot cta + seg, each with room for the
-// 8 (query token, head) columns of a group); at the very end of the
-// caller's buffer, one page ticket per segment.  Only the tickets must be
-// zero when a call starts, and a completed call leaves them at zero.  The
-// partials' size grows with the batch and the tickets sit at the end, so a
-// workspace sized for batch B serves every call with the same descriptor and
-// a batch of at most B: a smaller call's tickets are the tail of a larger
-// call's, and no call's partials reach the tickets of any batch up to B.
+// (query token, head) columns of a group: 8, or group x query tokens when
+// that is more); at the very end of the caller's buffer, one page ticket per
+// segment.  Only the tickets must be zero when a call starts, and a completed
+// call leaves them at zero.  The partials' size grows with the batch and the
+// columns and the tickets sit at the end, so a workspace sized for batch B
+// and q_len Q serves every call with the same descriptor, a batch of at most
+// B and at most Q query tokens: a smaller call's tickets are the tail of a
+// larger call's, and no call's partials reach the tickets of any such call.
+int nc_of(const pkv_cache_desc* d, int32_t qlen) {
+  const int g = d->num_q_heads / d->num_kv_heads;
+  const int qc = qlen <= 1 ? 1 : (qlen <= 2 ? 2 : (qlen <= 4 ? 4 : 8));
+  return g * qc;
+}
 WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t hint,
-                   int num_sms) {
-  // partial slots hold up to 8 (query token, head) columns, whatever the call
-  const int64_t g = 8;
+                   int num_sms, int nc) {
+  const int64_t g = pkv::decode_part_cols(nc);
   const int64_t cap = (int64_t)mbs * kPageSize;
   const int64_t len = (hint > 0 && hint < cap) ? hint : cap;
   const int64_t np_max = (len + kPageSize - 1) / kPageSize;
@@ -145,7 +150,7 @@ cudaError_t decode_workspace_clear(void* workspace, size_t workspace_bytes,
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const WsLayout w = ws_layout(d, batch, mbs, hint, sms);
+  const WsLayout w = ws_layout(d, batch, mbs, hint, sms, nc_of(d, 1));
   char* ws = static_cast<char*>(workspace);
   return cudaMemsetAsync(ws + ticket_offset(workspace_bytes, w), 0, w.ticket_bytes, stream);
 }
@@ -189,7 +194,7 @@ pkv_status decode_checks(const pkv_cache_desc* desc, const void* q, const void* 
                          const int32_t* context_lens, int32_t batch, int32_t max_blocks_per_seq,
                          int32_t max_context_len_hint, float scale, const void* out,
                          pkv_dtype q_dtype, pkv_dtype out_dtype, const void* workspace,
-                         size_t workspace_bytes) {
+                         size_t workspace_bytes, int32_t qlen = 1) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if (batch < 0 || max_blocks_per_seq <= 0 || max_context_len_hint < 0)
@@ -208,12 +213,15 @@ pkv_status decode_checks(const pkv_cache_desc* desc, const void* q, const void* 
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return PKV_ERR_INVALID_ARG;
+  if (qlen < 1 || qlen > 8) return PKV_ERR_UNSUPPORTED;
   const pkv::CacheKind cache = kind_of(desc->cache_dtype);
-  if (pkv::decode_smem_bytes(desc->head_dim, cache, batch) > 227 * 1024)
-    return PKV_ERR_UNSUPPORTED;
+  const int nc = nc_of(desc, qlen);
+  const size_t smem = qlen == 1 ? pkv::decode_smem_bytes(desc->head_dim, cache, batch)
+                                 : pkv::mq_smem_bytes(desc->head_dim, cache, batch, nc);
+  if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
   const int sms = sm_count_current_device();
   if (sms <= 0) return PKV_ERR_CUDA;
-  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms);
+  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms, nc);
   if (workspace == nullptr || workspace_bytes < w.total || !aligned(workspace, 256))
     return PKV_ERR_WORKSPACE;
   return PKV_OK;
@@ -247,10 +255,11 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
                        int trigger_next = 0) {
   pkv_status st = decode_checks(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                                 max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype,
-                                out_dtype, workspace, workspace_bytes);
+                                out_dtype, workspace, workspace_bytes, qlen);
   if (st != PKV_OK || batch == 0) return st;
   const int sms = sm_count_current_device();
-  const WsLayout w = ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms);
+  const WsLayout w =
+      ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms, nc_of(desc, qlen));
   pkv::DecodeLaunch l;
   st = encode_cache_map(&l.tmap_k, k_cache, desc);
   if (st != PKV_OK) return st;
@@ -287,12 +296,8 @@ pkv_status decode_impl(const pkv_cache_desc* desc, const void* q, const void* k_
   l.p.scale_log2 = scale * 1.4426950408889634f;
   l.group = desc->num_q_heads / desc->num_kv_heads;
   // query-token capacity of the kernel: 1, or the smallest of 2, 4, 8 that
-  // holds qlen with group * capacity <= 8
-  l.qcap = 1;
-  if (qlen > 1) {
-    l.qcap = qlen <= 2 ? 2 : (qlen <= 4 ? 4 : 8);
-    if (l.group * l.qcap > 8) return PKV_ERR_UNSUPPORTED;
-  }
+  // holds qlen
+  l.qcap = nc_of(desc, qlen) / l.group;
   l.cache = kind_of(desc->cache_dtype);
   l.q_bf16 = (q_dtype == PKV_BF16);
   l.ctas = w.ctas;
@@ -383,11 +388,20 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* desc, void* k_cache, void* v_ca
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t max_blocks_per_seq, int32_t max_context_len_hint) {
+  return pkv_decode_workspace_bytes_multi(desc, batch, 1, max_blocks_per_seq,
+                                          max_context_len_hint);
+}
+
+size_t pkv_decode_workspace_bytes_multi(const pkv_cache_desc* desc, int32_t batch,
+                                        int32_t q_len, int32_t max_blocks_per_seq,
+                                        int32_t max_context_len_hint) {
   if (check_desc(desc) != PKV_OK || batch < 0 || max_blocks_per_seq <= 0) return 0;
+  if (q_len < 1 || q_len > 8) return 0;
   if (batch == 0) return 0;
   const int sms = sm_count_current_device();
   if (sms <= 0) return 0;
-  return ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms).total;
+  return ws_layout(desc, batch, max_blocks_per_seq, max_context_len_hint, sms,
+                   nc_of(desc, q_len)).total;
 }
 
 pkv_status pkv_paged_decode_attention(const pkv_cache_desc* desc, const void* q,
@@ -411,7 +425,7 @@ pkv_status pkv_paged_decode_attention_multi(
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if (q_len < 1) return PKV_ERR_INVALID_ARG;
-  if ((desc->num_q_heads / desc->num_kv_heads) * q_len > 8) return PKV_ERR_UNSUPPORTED;
+  if (q_len > 8) return PKV_ERR_UNSUPPORTED;
   return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                      max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
                      workspace, workspace_bytes, stream, /*early_prologue=*/0, q_len);
@@ -426,7 +440,7 @@ pkv_status pkv_paged_decode_attention_window(
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if (q_len < 1 || window < 0 || sinks < 0) return PKV_ERR_INVALID_ARG;
-  if ((desc->num_q_heads / desc->num_kv_heads) * q_len > 8) return PKV_ERR_UNSUPPORTED;
+  if (q_len > 8) return PKV_ERR_UNSUPPORTED;
   return decode_impl(desc, q, k_cache, v_cache, block_tables, context_lens, batch,
                      max_blocks_per_seq, max_context_len_hint, scale, out, q_dtype, out_dtype,
                      workspace, workspace_bytes, stream, /*early_prologue=*/0, q_len, window,

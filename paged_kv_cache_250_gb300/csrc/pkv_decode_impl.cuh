@@ -134,6 +134,8 @@ __device__ __forceinline__ void store_out_rt(pkv_dtype t, void* base, int64_t id
 // G query heads share a KV head; QC is the number of query tokens per
 // sequence the kernel is built for (p.qlen <= QC of them are real).  The
 // MMA's 8 columns hold the NC = QC * G (query token, head) pairs of a group.
+// The library builds it for one query token (QC = 1); several query tokens
+// per sequence go to the kernel of pkv_decode_mq.cuh.
 template <int D, int G, int QC, int CACHE, bool QBF16>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
@@ -1221,24 +1223,6 @@ cudaError_t dispatch_split(const DecodeLaunch& l) {
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   }
   PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
-#undef PKV_CASE
-  return cudaErrorNotSupported;
-}
-
-// Several query tokens per sequence (l.qcap = 2, 4 or 8, with group * qcap <= 8).
-template <int CACHE, bool QBF16>
-cudaError_t dispatch_split_multi(const DecodeLaunch& l) {
-  const int d = l.p.d;
-  const int g = l.group;
-  const int qc = l.qcap;
-#define PKV_CASE(DD, GG, QQ) \
-  if (d == DD && g == GG && qc == QQ) return launch_split<DD, GG, QQ, CACHE, QBF16>(l);
-  if constexpr (!cache_is_fp8((CacheKind)CACHE)) {
-    PKV_CASE(64, 1, 2) PKV_CASE(64, 1, 4) PKV_CASE(64, 1, 8)
-    PKV_CASE(64, 2, 2) PKV_CASE(64, 2, 4) PKV_CASE(64, 4, 2)
-  }
-  PKV_CASE(128, 1, 2) PKV_CASE(128, 1, 4) PKV_CASE(128, 1, 8)
-  PKV_CASE(128, 2, 2) PKV_CASE(128, 2, 4) PKV_CASE(128, 4, 2)
 #undef PKV_CASE
   return cudaErrorNotSupported;
 }

@@ -29,18 +29,19 @@ constexpr int kRangeMax = 64;
 // cut (a state merge, an output write and a pipeline refill).
 constexpr int kSegCost = 12;
 
-// Shared-memory plan of the decode kernel (host and device agree on it).
-constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
-constexpr int decode_stage_bytes(int d, CacheKind c) {
+// Shared-memory plan of the single-token decode kernel (pkv_decode_impl.cuh;
+// host and device agree on it).
+__host__ __device__ constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
+__host__ __device__ constexpr int decode_stage_bytes(int d, CacheKind c) {
   return 2 * kPageSize * d * (cache_is_fp8(c) ? 1 : 2);
 }
 // per-token scales of one staged page (K then V), kept beside the page ring
-constexpr int decode_scale_bytes(CacheKind c) {
+__host__ __device__ constexpr int decode_scale_bytes(CacheKind c) {
   return c == kCacheE4M3Tok ? 2 * kPageSize * 4 : 0;
 }
 // alignment slack + descriptor rings + merge buffers + merge flags +
 // mbarriers (8 stages max per warp, 4 slots for the flush hand-off)
-constexpr int decode_fixed_smem(int d) {
+__host__ __device__ constexpr int decode_fixed_smem(int d) {
   return 1024 + kDecodeWarps * 64 * 8 + 2 * decode_lane_state(d) * 32 * 4 +
          2 * kDecodeWarps * 4 + kDecodeWarps * 8 * 8 + 32;
 }
@@ -48,10 +49,47 @@ constexpr int decode_fixed_smem(int d) {
 // per SM, 1 KB reserved per CTA) with room for the per-sequence arrays of a
 // 128-sequence batch; between 2 and 8.
 constexpr int kDecodeSmemTarget = 113 * 1024;
-constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
-constexpr int decode_stages(int d, CacheKind c) {
+__host__ __device__ constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
+__host__ __device__ constexpr int decode_stages(int d, CacheKind c) {
   return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d) - 2600) /
                              (kDecodeWarps * (decode_stage_bytes(d, c) + decode_scale_bytes(c))));
+}
+
+// Columns of the multi-query kernel (pkv_decode_mq.cuh) built for nc (query
+// token, head) pairs per KV head (nc = group x query tokens, a power of two
+// from 2 to 64): MMA column groups of 8, cw of them per warp, and sl warps
+// ("slices") that compute disjoint column ranges of every page; the other
+// kDecodeWarps / sl warps of a slice share its pages.
+__host__ __device__ constexpr int mq_cw(int nc) { return nc <= 8 ? 1 : 2; }
+__host__ __device__ constexpr int mq_sl(int nc) { return nc <= 16 ? 1 : nc / 16; }
+// columns a partial slot holds (at least 8, whatever the call)
+__host__ __device__ constexpr int decode_part_cols(int nc) { return nc < 8 ? 8 : nc; }
+// floats of one warp's online-softmax state per lane: (m, l) for two
+// columns and O^T fragments, per column group
+__host__ __device__ constexpr int mq_lane_state(int d, int nc) {
+  return mq_cw(nc) * (4 + 4 * (d / 16));
+}
+// merge buffers: two warp states (none when every warp owns its columns)
+__host__ __device__ constexpr int mq_mbuf_bytes(int d, int nc) {
+  return mq_sl(nc) == kDecodeWarps ? 0 : 2 * mq_lane_state(d, nc) * 32 * 4;
+}
+constexpr int kDescN = 128;      // page descriptors (int4) in the CTA's ring
+constexpr int kDescBlock = 32;   // descriptors written by one fill (one per lane)
+constexpr int kSmemInts = 96;    // flags, counters, merge flags, ordinal issued per slot
+constexpr int kFlushBars = 16;   // mbarriers of the segment-end hand-off
+// bytes per ring slot: the K and V page, their per-token scales, the slot's
+// mbarrier and its pending-consumer count
+__host__ __device__ constexpr int mq_slot_bytes(int d, CacheKind c) {
+  return decode_stage_bytes(d, c) + decode_scale_bytes(c) + 8 + 4;
+}
+__host__ __device__ constexpr int mq_fixed_smem(int d, int nc) {
+  return 1024 + kFlushBars * 8 + 16 + kDescN * 16 + mq_mbuf_bytes(d, nc) + kSmemInts * 4;
+}
+// Ring slots of a CTA: as many K+V pages as fit two CTAs per SM with room for
+// the per-sequence arrays of a 128-sequence batch; between 4 and 28.
+__host__ __device__ constexpr int mq_clamp_ring(int r) { return r < 4 ? 4 : (r > 28 ? 28 : r); }
+__host__ __device__ constexpr int mq_ring(int d, CacheKind c, int nc) {
+  return mq_clamp_ring((kDecodeSmemTarget - mq_fixed_smem(d, nc) - 2600) / mq_slot_bytes(d, c));
 }
 
 // Arguments of the decode kernel (one CTA = one contiguous share of all
@@ -61,9 +99,9 @@ struct DecodeParams {
   const int32_t* block_tables; // [B][MBS]
   const int32_t* context_lens; // [B]
   void* out;                   // [B][Hq][d]
-  float* part_o;               // [max ctas+B*Hkv][G][d] unnormalised partial outputs
-  float* part_ml;              // [max ctas+B*Hkv][G][2] (reference max in log2 units, sum)
-  int32_t* tickets;            // [B*Hkv]            pages stored per segment; zero between calls
+  float* part_o;               // [max ctas+B*Hkv][cols][d] unnormalised partial outputs
+  float* part_ml;              // [max ctas+B*Hkv][cols][2] (reference max in log2 units, sum)
+  int32_t* tickets;            // [B*Hkv]  pages stored per segment (x slices); zero between calls
   const float* k_scale;        // FP8 only
   const float* v_scale;        // FP8 only
   int32_t* err_word;
@@ -87,7 +125,7 @@ struct DecodeLaunch {
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
   int32_t group;               // Hq / Hkv
-  int32_t qcap;                // query tokens the kernel is built for (>= p.qlen)
+  int32_t qcap;                // query tokens the kernel is built for (>= p.qlen; 1, 2, 4, 8)
   CacheKind cache;
   bool q_bf16;
   int32_t ctas;
@@ -111,11 +149,17 @@ struct AppendParams {
   int32_t T, Hkv, d, NB;
 };
 
-// Dynamic shared memory the split kernel needs for a batch of B sequences.
+// Dynamic shared memory the single-token kernel needs for a batch of B
+// sequences.
 inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
   return (size_t)decode_fixed_smem(d) +
          (size_t)kDecodeWarps * decode_stages(d, cache) *
              (decode_stage_bytes(d, cache) + decode_scale_bytes(cache)) +
+         (size_t)(5 * B + 2) * 4;
+}
+// The same for the multi-query kernel built for nc columns.
+inline size_t mq_smem_bytes(int32_t d, CacheKind cache, int32_t B, int32_t nc) {
+  return (size_t)mq_fixed_smem(d, nc) + (size_t)mq_ring(d, cache, nc) * mq_slot_bytes(d, cache) +
          (size_t)(5 * B + 2) * 4;
 }
 
@@ -129,6 +173,10 @@ cudaError_t launch_decode_multi_f16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_bf16(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_e4m3(const DecodeLaunch& l);
 cudaError_t launch_decode_multi_e4m3_tok(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_f16_d64(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_bf16_d64(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_e4m3_f16q(const DecodeLaunch& l);
+cudaError_t launch_decode_multi_e4m3_tok_f16q(const DecodeLaunch& l);
 // The argument checks of pkv_paged_decode_attention, with nothing launched.
 pkv_status decode_validate(const pkv_cache_desc* desc, const void* q, const void* k_cache,
                            const void* v_cache, const int32_t* block_tables,

@@ -179,3 +179,26 @@ def assert_close(got: np.ndarray, ref: np.ndarray, cfg, out_dtype: str, what: st
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of bound; max abs err "
                            f"{err.max():.3e} (tol {tol})")
     return float(err.max())
+
+
+def assert_same_rounding(a, b, what: str = ""):
+    """Two runs of the same decode: equal up to the order in which fp32
+    partial sums were added (each page goes to whichever warp is free, so
+    runs differ in the last bits).  fp32 outputs within 1e-5 + 1e-5 |a|
+    (reordering a few thousand fp32 terms moves a sum by ~1e-6); 16-bit
+    outputs within one unit in the last place of their type."""
+    if isinstance(a, torch.Tensor):
+        dt = a.dtype
+        a = a.double().cpu().numpy()
+        b = b.double().cpu().numpy()
+    else:
+        dt = torch.float32
+    assert a.shape == b.shape
+    assert np.array_equal(np.isfinite(a), np.isfinite(b)), f"{what}: finiteness differs"
+    d = np.abs(a - b)
+    if dt == torch.float32:
+        bound = 1e-5 + 1e-5 * np.abs(a)
+    else:
+        bound = 2 * half_ulp(np.maximum(np.abs(a), np.abs(b)), dt)
+    bad = d > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements differ beyond rounding; max {d.max():.3e}"

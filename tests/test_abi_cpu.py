@@ -132,13 +132,20 @@ def test_argument_errors_of_the_later_entry_points():
                                                    window, sinks, 4, 0, 1.0, fake, pkv.PKV_BF16,
                                                    pkv.PKV_F32, fake, 1 << 20, None)
         assert st == pkv.PKV_ERR_INVALID_ARG
-    # multi-query: q_len 0; more (token, head) columns than the 8 built
+    # multi-query: q_len 0; more query tokens than the 8 built (at any group)
     st = lib.pkv_paged_decode_attention_multi(D, fake, fake, fake, fake, fake, 2, 0, 4, 0, 1.0,
                                               fake, pkv.PKV_BF16, pkv.PKV_F32, fake, 1 << 20, None)
     assert st == pkv.PKV_ERR_INVALID_ARG
-    st = lib.pkv_paged_decode_attention_multi(D, fake, fake, fake, fake, fake, 2, 3, 4, 0, 1.0,
+    st = lib.pkv_paged_decode_attention_multi(D, fake, fake, fake, fake, fake, 2, 9, 4, 0, 1.0,
                                               fake, pkv.PKV_BF16, pkv.PKV_F32, fake, 1 << 20, None)
-    assert st == pkv.PKV_ERR_UNSUPPORTED  # group 4 x 3 tokens > 8
+    assert st == pkv.PKV_ERR_UNSUPPORTED
+    st = lib.pkv_paged_decode_attention_window(D, fake, fake, fake, fake, fake, 2, 9, 100, 4, 4,
+                                               0, 1.0, fake, pkv.PKV_BF16, pkv.PKV_F32, fake,
+                                               1 << 20, None)
+    assert st == pkv.PKV_ERR_UNSUPPORTED
+    # the multi-query workspace size refuses q_len outside 1 .. 8
+    assert lib.pkv_decode_workspace_bytes_multi(D, 2, 0, 4, 0) == 0
+    assert lib.pkv_decode_workspace_bytes_multi(D, 2, 9, 4, 0) == 0
     # one-kernel step: a null q; an empty batch is a no-op
     st = lib.pkv_decode_step_fused(D, None, fake, fake, fake, fake, pkv.PKV_BF16, fake, fake, 2,
                                    4, 0, 1.0, fake, pkv.PKV_BF16, pkv.PKV_F32, fake, 1 << 20, 0,

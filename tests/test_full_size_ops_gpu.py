@@ -29,6 +29,10 @@ def _launch(name, q_len, window=None, sinks=0, seed=0):
     w = wl.generate(cfg, device="cuda")
     run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
     run.append()
+    # the bench's workspace: partials of group x q_len columns
+    n = pkv.pkv_decode_workspace_bytes_multi(run.desc, cfg.batch, q_len, w.max_blocks_per_seq,
+                                             run.hint)
+    run.workspace = torch.zeros(n, dtype=torch.uint8, device="cuda")
     g = torch.Generator().manual_seed(400 + seed)
     q = torch.randn(cfg.batch, q_len, cfg.q_heads, cfg.head_dim, generator=g).to(cfg.qdt)
     out = torch.empty(cfg.batch, q_len, cfg.q_heads, cfg.head_dim, dtype=torch.bfloat16,
@@ -57,6 +61,8 @@ def _sampled_pairs(cfg, w, rng, n_extra=4, heads=2):
     ("mha_7b_b64_ctx8192_bf16", 8),        # g 1: eight tokens fill the MMA's columns
     ("llama3_8b_b32_ctx1-4096_bf16", 2),   # g 4 x 2 tokens, ragged lengths, length hint
     ("llama3_70b_b8_ctx32768_bf16", 1),    # g 8, one token: the multi-query call's QC 1 form
+    ("llama3_70b_b8_ctx32768_bf16", 4),    # g 8 x 4 tokens: 32 columns over two slices
+    ("llama3_8b_b32_ctx1-4096_bf16", 5),   # g 4 x 5 tokens (capacity 8): 32 columns
 ])
 def test_multi_query_full_size_sampled(name, q_len):
     cfg, w, q, got = _launch(name, q_len, seed=1)
@@ -75,6 +81,7 @@ def test_multi_query_full_size_sampled(name, q_len):
 @pytest.mark.parametrize("name,q_len,window,sinks", [
     ("mha_7b_b64_ctx8192_bf16", 2, 4096, 4),      # the windowed bench line
     ("llama3_8b_b32_ctx1-4096_bf16", 1, 1000, 16),  # windows shorter than many contexts
+    ("llama3_70b_b8_ctx32768_bf16", 4, 4096, 4),    # 32 columns under a window
 ])
 def test_window_full_size_sampled(name, q_len, window, sinks):
     cfg, w, q, got = _launch(name, q_len, window, sinks, seed=2)
