@@ -17,14 +17,16 @@
 // equal cost (at least kRangeMin each), one per CTA of a persistent grid (two
 // CTAs per SM), so ragged lengths never leave an SM idle.  A CTA walks its
 // share in pieces of at most kRangeMax pages; page j of a piece goes to warp
-// j % 4, so the four warps move through the same segment together, each with
-// its own online-softmax state, taking two of their pages per step.
+// j % NW (NW = 4 warps per CTA for 16-bit caches, 6 for E4M3, whose byte
+// conversions want more warps to hide their latency), so the warps move
+// through the same segment together, each with its own online-softmax state,
+// taking one or two of their pages per step.
 //
-// Segment ends.  The four warp states are merged when the share leaves a
+// Segment ends.  The NW warp states are merged when the share leaves a
 // segment (the merge is order-independent): for groups of up to 4 query
-// heads three warps hand their state over through shared memory and an
-// mbarrier and keep streaming while a rotating fourth merges and writes; for
-// groups of 8 a tree of CTA barriers does it.  A segment wholly inside one
+// heads NW - 1 warps hand their state over through shared memory and an
+// mbarrier and keep streaming while a rotating last one merges and writes;
+// for groups of 8 a tree of CTA barriers does it.  A segment wholly inside one
 // share is normalised and written at once; a segment cut by share boundaries
 // gets one partial (m, l, o) per CTA, in slot cta + segment, and a page-count
 // ticket; the CTA whose pages complete the segment merges the partials (the
@@ -67,7 +69,6 @@ namespace pkv {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr int kMergeBarrier = 1;                  // named barrier id (0 = __syncthreads)
-constexpr int kDescRing = 64;                     // page descriptors per warp
 // A descriptor holds the tokens from the page's start to the context's end,
 // capped here (enough for the causal limits of up to 8 query tokens).
 constexpr int kRemCap = 2 * kPageSize;
@@ -102,8 +103,9 @@ __device__ __forceinline__ uint32_t swz(int tok, int chunk) {
                     (((chunk & 7) ^ (tok & 7)) << 4));
 }
 
+template <int NW>
 __device__ __forceinline__ void merge_barrier() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kMergeBarrier), "n"(kDecodeWarps * 32) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"n"(kMergeBarrier), "n"(NW * 32) : "memory");
 }
 
 __device__ __forceinline__ void griddep_wait() {
@@ -137,7 +139,7 @@ __device__ __forceinline__ void store_out_rt(pkv_dtype t, void* base, int64_t id
 // The library builds it for one query token (QC = 1); several query tokens
 // per sequence go to the kernel of pkv_decode_mq.cuh.
 template <int D, int G, int QC, int CACHE, bool QBF16>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
+__global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCtasPerSm)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
   constexpr int NC = G * QC;
@@ -145,7 +147,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   using C = DecodeCfg<D, CACHE>;
   constexpr bool kBF = (CACHE == kCacheBF16);  // mma operand type (else fp16)
   constexpr int kS = C::kStages;
-  constexpr int NW = kDecodeWarps;
+  constexpr int NW = decode_warps((CacheKind)CACHE);
+  constexpr int kDescRing = decode_desc_ring(NW);  // page descriptors per warp
+  static_assert(2 * ((kRangeMax + NW - 1) / NW) <= kDescRing, "two pieces per ring");
+  constexpr int kMbuf = decode_mbuf_floats(D, NW);
+  auto merge_barrier = [] { pkv::merge_barrier<NW>(); };
   constexpr int kMT = C::kMTiles;
   // pages a warp takes per step: 2 on rings of 3+ pages (4 measured slower:
   // longer P.V accumulation chains)
@@ -179,8 +185,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   static_assert((NW * kS * 8) % 16 == 0 && (NW * kDescRing * 8) % 16 == 0, "smem alignment");
   int2* desc_all = reinterpret_cast<int2*>(fbar + 4);    // [NW][kDescRing]
   int2* desc = desc_all + warp * kDescRing;
-  float* mbuf = reinterpret_cast<float*>(desc_all + NW * kDescRing);  // [2][kLaneState][32]
-  int* mflag = reinterpret_cast<int*>(mbuf + 2 * C::kLaneState * 32);  // [2 NW] merges due
+  float* mbuf = reinterpret_cast<float*>(desc_all + NW * kDescRing);  // [kMbuf]
+  int* mflag = reinterpret_cast<int*>(mbuf + kMbuf);                   // [2 NW] merges due
   int32_t* pfx = mflag + 2 * NW;                                      // [B+1] pages
   int32_t* nzp = pfx + (p.B + 1);                                     // [B+1] non-empty seqs
   int32_t* ctxs = nzp + (p.B + 1);                                    // [B]
@@ -299,9 +305,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
     return a;
   };
-  // The warp's pages of piece [s, e) are s + warp + 4j; ordinals continue
-  // across pieces; desc[] holds 64 ordinals (two pieces of at most
-  // kRangeMax / 4 = 16 pages per warp each).
+  // The warp's pages of piece [s, e) are s + warp + NW j; ordinals continue
+  // across pieces; desc[] holds kDescRing ordinals (at least two pieces of
+  // at most ceil(kRangeMax / NW) pages per warp each).
   auto warp_count = [&](int2 r) -> int {
     const int n = r.y - r.x - warp;
     return n > 0 ? (n + NW - 1) / NW : 0;
@@ -997,28 +1003,32 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   };
 
   // ---- end of this CTA's part of a segment.  The warp that finishes (merges
-  // the four states and writes) rotates from flush to flush.
-  // Synchronous form (used when three warp states do not fit in mbuf): a
-  // tree of CTA barriers.
+  // the NW states and writes) rotates from flush to flush.
+  // Synchronous form (used when the other warps' compact states do not fit
+  // in mbuf): a tree of CTA barriers over two state buffers; each round the
+  // two highest roles left hand their states to roles 0 and 1.
   auto flush_sync = [&](int b, int h, bool split, int pages_mine) {
     float* buf0 = mbuf;
     float* buf1 = mbuf + C::kLaneState * 32;
-    const int wr = (warp - nflushes) & (NW - 1);  // this warp's role
+    const int wr = (warp + NW - nflushes % NW) % NW;  // this warp's role
     ++nflushes;
     tickets_step(false);
     merge_barrier();
     merge_flagged();  // uses mbuf, before the states go there
-    if (wr >= 2) store_state(wr == 2 ? buf0 : buf1);
-    merge_barrier();
-    if (wr < 2) merge_state(wr == 0 ? buf0 : buf1);
-    merge_barrier();
+#pragma unroll
+    for (int n = NW; n > 2; n -= 2) {
+      if (wr >= n - 2 && wr < n) store_state(wr == n - 2 ? buf0 : buf1);
+      merge_barrier();
+      if (wr < 2) merge_state(wr == 0 ? buf0 : buf1);
+      merge_barrier();
+    }
     if (wr == 1) store_state(buf0);
     merge_barrier();
     if (wr != 0) return;
     merge_state(buf0);
     finish(b, h, split, pages_mine);
   };
-  // Asynchronous form (NC <= 4): the three other warps drop the lanes of their
+  // Asynchronous form (NC <= 4): the NW - 1 other warps drop the lanes of their
   // state that hold real heads into mbuf slots, arrive on the "full"
   // mbarrier and go on with the next segment at once, so their copies keep
   // streaming; the finisher waits on "full", merges, frees the slots through
@@ -1033,10 +1043,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
   // waited for by the warps whose arrivals complete phase n - 1.
   constexpr int kU = NC >= 4 ? NC / 2 : 1;     // C-fragment column pairs with real columns
   constexpr int kCS = C::kLaneState * 8 * kU;  // floats per compact warp state
-  constexpr bool kAsyncFlush = NC <= 4 && (NW - 1) * kCS <= 2 * C::kLaneState * 32;
+  constexpr bool kAsyncFlush = NC <= 4 && (NW - 1) * kCS <= kMbuf;
   auto flush_async = [&](int b, int h, bool split, int pages_mine) {
     const int n = nflushes++;
-    const int fin = n & (NW - 1);
+    const int fin = n % NW;
     const uint32_t bar_full = smem_u32(fbar + (n & 1)), bar_empty = smem_u32(fbar + 2);
     int m0 = -1, m1 = -1;
     if (lane == 0) tickets_lane0(false, m0, m1);
@@ -1049,7 +1059,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     if (warp != fin) {
       if (n > 0 && !dead && !mbar_wait_bounded(bar_empty, (uint32_t)((n - 1) & 1), kWaitLimitNs))
         set_dead(k);
-      if (c4 < kU) store_state_at(mbuf + ((warp - fin - 1) & (NW - 1)) * kCS, li, 8 * kU);
+      if (c4 < kU) store_state_at(mbuf + ((warp - fin - 1 + NW) % NW) * kCS, li, 8 * kU);
       mbar_arrive(bar_full);
       return;
     }
@@ -1201,7 +1211,7 @@ cudaError_t launch_split(const DecodeLaunch& l) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)l.ctas);
-  cfg.blockDim = dim3(kDecodeWarps * 32);
+  cfg.blockDim = dim3(decode_warps((CacheKind)CACHE) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[1];

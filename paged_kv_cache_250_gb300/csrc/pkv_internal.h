@@ -11,7 +11,9 @@
 namespace pkv {
 
 constexpr int kPageSize = 16;  // tokens per block: the only page size built
-constexpr int kDecodeWarps = 4;
+constexpr int kDecodeWarps = 4;     // warps per CTA of the 16-bit and multi-query kernels
+constexpr int kDecodeWarpsFp8 = 6;  // of the single-token E4M3 kernel (more warps hide
+                                    // the latency of the byte-to-fp16 conversions)
 constexpr int kDecodeCtasPerSm = 2;
 
 // E4M3: one fp32 scale per KV head; E4M3 per token: one K and one V scale per
@@ -31,7 +33,21 @@ constexpr int kSegCost = 12;
 
 // Shared-memory plan of the single-token decode kernel (pkv_decode_impl.cuh;
 // host and device agree on it).
+__host__ __device__ constexpr int decode_warps(CacheKind c) {
+  return cache_is_fp8(c) ? kDecodeWarpsFp8 : kDecodeWarps;
+}
+// page descriptors per warp: two pieces of at most ceil(kRangeMax / warps)
+// pages each, rounded up to a power of two
+__host__ __device__ constexpr int decode_desc_ring(int nw) { return nw <= 4 ? 64 : 32; }
 __host__ __device__ constexpr int decode_lane_state(int d) { return 4 + 4 * (d / 16); }
+// merge buffer (floats): two whole warp states for the barrier tree, or the
+// compact states (two column pairs each) of all warps but one for the
+// asynchronous hand-off
+__host__ __device__ constexpr int decode_mbuf_floats(int d, int nw) {
+  return 2 * decode_lane_state(d) * 32 > (nw - 1) * decode_lane_state(d) * 16
+             ? 2 * decode_lane_state(d) * 32
+             : (nw - 1) * decode_lane_state(d) * 16;
+}
 __host__ __device__ constexpr int decode_stage_bytes(int d, CacheKind c) {
   return 2 * kPageSize * d * (cache_is_fp8(c) ? 1 : 2);
 }
@@ -41,9 +57,10 @@ __host__ __device__ constexpr int decode_scale_bytes(CacheKind c) {
 }
 // alignment slack + descriptor rings + merge buffers + merge flags +
 // mbarriers (8 stages max per warp, 4 slots for the flush hand-off)
-__host__ __device__ constexpr int decode_fixed_smem(int d) {
-  return 1024 + kDecodeWarps * 64 * 8 + 2 * decode_lane_state(d) * 32 * 4 +
-         2 * kDecodeWarps * 4 + kDecodeWarps * 8 * 8 + 32;
+__host__ __device__ constexpr int decode_fixed_smem(int d, CacheKind c) {
+  return 1024 + decode_warps(c) * decode_desc_ring(decode_warps(c)) * 8 +
+         decode_mbuf_floats(d, decode_warps(c)) * 4 + 2 * decode_warps(c) * 4 +
+         decode_warps(c) * 8 * 8 + 32;
 }
 // Ring depth: as many K+V page slots per warp as fit two CTAs per SM (228 KB
 // per SM, 1 KB reserved per CTA) with room for the per-sequence arrays of a
@@ -51,8 +68,8 @@ __host__ __device__ constexpr int decode_fixed_smem(int d) {
 constexpr int kDecodeSmemTarget = 113 * 1024;
 __host__ __device__ constexpr int decode_clamp_stages(int s) { return s < 2 ? 2 : (s > 8 ? 8 : s); }
 __host__ __device__ constexpr int decode_stages(int d, CacheKind c) {
-  return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d) - 2600) /
-                             (kDecodeWarps * (decode_stage_bytes(d, c) + decode_scale_bytes(c))));
+  return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem(d, c) - 2600) /
+                             (decode_warps(c) * (decode_stage_bytes(d, c) + decode_scale_bytes(c))));
 }
 
 // Columns of the multi-query kernel (pkv_decode_mq.cuh) built for nc (query
@@ -152,8 +169,8 @@ struct AppendParams {
 // Dynamic shared memory the single-token kernel needs for a batch of B
 // sequences.
 inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
-  return (size_t)decode_fixed_smem(d) +
-         (size_t)kDecodeWarps * decode_stages(d, cache) *
+  return (size_t)decode_fixed_smem(d, cache) +
+         (size_t)decode_warps(cache) * decode_stages(d, cache) *
              (decode_stage_bytes(d, cache) + decode_scale_bytes(cache)) +
          (size_t)(5 * B + 2) * 4;
 }
