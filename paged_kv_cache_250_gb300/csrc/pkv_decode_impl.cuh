@@ -584,25 +584,29 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
     for (int e = 0; e < 4; ++e) s[e] += s2[e];
   };
 
-  // ---- O^T += V^T . P^T for one page; V rows of masked tokens are zeroed
-  // (they may hold anything, and 0 * NaN would poison the sum)
-  auto pv_page = [&](uint32_t vt, int valid, uint32_t bh0, uint32_t bh1, uint32_t bl0,
-                     uint32_t bl1) {
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-    if (valid < kPageSize) {
-      const int t0 = 2 * c4;
-      mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-      mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+  // ---- V rows at and past the context's end may hold anything (a stale or
+  // never-written slot, and 0 * NaN would poison P.V): the last page of a
+  // segment gets them zeroed in its staged copy, so P.V needs no mask.  The
+  // slot is refilled by the tensor-copy (async) proxy later.
+  auto zero_tail = [&](uint32_t vt, int rem) {
+    const int n = (kPageSize - rem) * C::kBoxes * 8;  // 16-byte chunks: (row, box, chunk)
+    for (int i = lane; i < n; i += 32) {
+      const int row = rem + i / (C::kBoxes * 8);
+      const int bx = (i / 8) % C::kBoxes;
+      const uint32_t a = vt + (uint32_t)(bx * C::kBoxBytes + row * 128 + (i % 8) * 16);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
     }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+  };
+
+  // ---- O^T += V^T . P^T for one page
+  auto pv_page = [&](uint32_t vt, uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
     if constexpr (!kFp8) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         uint32_t a[4];
         ldsm_x4_trans(a, vt + swz(pv_tok, 2 * mt + pv_chunk_hi));
-        a[0] &= mlo;
-        a[1] &= mlo;
-        a[2] &= mhi;
-        a[3] &= mhi;
         mma_16816<kBF>(o[mt], a, bh0, bh1);
         mma_16816<kBF>(o[mt], a, bl0, bl1);
       }
@@ -614,18 +618,10 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
         uint32_t a[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) a[e] = e4m3x2_to_f16x2(__byte_perm(r[e], 0, 0x0020));
-        a[0] &= mlo;
-        a[1] &= mlo;
-        a[2] &= mhi;
-        a[3] &= mhi;
         mma_16816<false>(o[2 * gi], a, bh0, bh1);
         mma_16816<false>(o[2 * gi], a, bl0, bl1);
 #pragma unroll
         for (int e = 0; e < 4; ++e) a[e] = e4m3x2_to_f16x2(__byte_perm(r[e], 0, 0x0031));
-        a[0] &= mlo;
-        a[1] &= mlo;
-        a[2] &= mhi;
-        a[3] &= mhi;
         mma_16816<false>(o[2 * gi + 1], a, bh0, bh1);
         mma_16816<false>(o[2 * gi + 1], a, bl0, bl1);
       }
@@ -752,8 +748,9 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
       const uint32_t l01 = pack2<kBF>(p0 - f01.x, p1 - f01.y);
       const uint32_t l23 = pack2<kBF>(p2 - f23.x, p3 - f23.y);
       const int vrows = valids[i] & kRemMask;
-      pv_page(kt[i] + C::kTileBytes, vrows < kPageSize ? vrows : kPageSize, movm_trans(h01),
-              movm_trans(h23), movm_trans(l01), movm_trans(l23));
+      if (vrows < kPageSize) zero_tail(kt[i] + C::kTileBytes, vrows);
+      pv_page(kt[i] + C::kTileBytes, movm_trans(h01), movm_trans(h23), movm_trans(l01),
+              movm_trans(l23));
     }
   };
   auto compute_page = [&](uint32_t kt, int valid) {
