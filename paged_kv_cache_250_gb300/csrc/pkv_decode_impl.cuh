@@ -279,18 +279,19 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
     }
     const int64_t np = pfx[a + 1] - pfx[a];
     const int64_t r = P - seq_cost0(a);
-    const int64_t hh = r / (np + kSegCost);
+    const int64_t hh = udiv64(r, np + kSegCost);
     const int64_t off = r - hh * (np + kSegCost) - kSegCost;
     return (int64_t)p.Hkv * pfx[a] + hh * np + (off > 0 ? off : 0);
   };
-  const int64_t sh_lo = blockIdx.x < Gs ? unit_at_cost((Tc * blockIdx.x + Gs - 1) / Gs) : W;
-  const int64_t sh_hi = blockIdx.x < Gs ? unit_at_cost((Tc * (blockIdx.x + 1) + Gs - 1) / Gs) : W;
+  const int64_t sh_lo = blockIdx.x < Gs ? unit_at_cost(udiv64(Tc * blockIdx.x + Gs - 1, Gs)) : W;
+  const int64_t sh_hi =
+      blockIdx.x < Gs ? unit_at_cost(udiv64(Tc * (blockIdx.x + 1) + Gs - 1, Gs)) : W;
   // the CTA whose share holds unit x of sequence b, KV head h
   auto cta_of = [&](int64_t x, int b, int64_t h) -> int64_t {
     const int64_t np = pfx[b + 1] - pfx[b];
     const int64_t start = (int64_t)p.Hkv * pfx[b] + h * np;
     const int64_t X = seq_cost0(b) + h * (np + kSegCost) + kSegCost + (x - start);
-    return X * Gs / Tc;
+    return udiv64(X * Gs, Tc);
   };
   auto piece = [&](int i) -> int2 {
     const int64_t s0 = sh_lo + (int64_t)i * kRangeMax;
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
       const int b = seq_of(x);
       const int np = pfx[b + 1] - pfx[b];
       const int64_t rr = x - (int64_t)p.Hkv * pfx[b];
-      const int h = (int)(rr / np);
+      const int h = (int)udiv64(rr, np);
       const int pgu = (int)(rr - (int64_t)h * np);  // unit within the segment
       const int pg = pgu < gns[b] ? pgu : pgu + gsk[b];
       const int blk = p.block_tables[(int64_t)b * p.MBS + pg];
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
       const int b = seq_of(x);
       const int np = pfx[b + 1] - pfx[b];
       const int64_t rr = x - (int64_t)p.Hkv * pfx[b];
-      f_h = (int)(rr / np);
+      f_h = (int)udiv64(rr, np);
       const int pgu = (int)(rr - (int64_t)f_h * np);  // unit within the segment
       const int pg = pgu < gns[b] ? pgu : pgu + gsk[b];
       f_blk = p.block_tables[(int64_t)b * p.MBS + pg];
@@ -411,8 +412,24 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
   fill_desc(r0, 0);
 
   // From here on the kernel touches data the previous kernel on the stream may
-  // write (cache pages, q, outputs, workspace): wait for it.
-  if (p.early_prologue) griddep_wait();
+  // write (cache pages, q, outputs, workspace): wait for it.  The warp's
+  // first pages (two ring fills for 16-bit caches, one for E4M3: measured
+  // best) start towards L2 before the wait (an L2 prefetch moves no data
+  // into the CTA; a row the previous kernel writes meanwhile lands in L2
+  // over the prefetched line, where the loads after the wait read it).
+  if (p.early_prologue) {
+    constexpr int kPrefetch = kFp8 ? kS : 2 * kS;
+    static_assert(kPrefetch <= 32, "one page per lane");
+    if (lane < kPrefetch && lane < warp_count(r0)) {
+      const int2 dsc = desc[lane];
+      if (dsc.x >= 0) {
+        const int64_t off = (int64_t)dsc.x * C::kRowBytes;
+        l2_prefetch_bulk(static_cast<const char*>(p.k_cache) + off, C::kTileBytes);
+        l2_prefetch_bulk(static_cast<const char*>(p.v_cache) + off, C::kTileBytes);
+      }
+    }
+    griddep_wait();
+  }
 
   int issued = 0;      // ordinals whose load was issued
   int filled_end = 0;  // ordinals with a descriptor
@@ -1088,7 +1105,7 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
       const int b = seq_of(x);
       const int np = pfx[b + 1] - pfx[b];
       const int64_t sb = (int64_t)p.Hkv * pfx[b];
-      const int h = (int)((x - sb) / np);
+      const int h = (int)udiv64(x - sb, np);
       const int64_t seg_start = sb + (int64_t)h * np;
       const int64_t seg_end = seg_start + np;
       const int64_t pe = seg_end < R.y ? seg_end : R.y;

@@ -99,6 +99,19 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
+// a / b for a >= 0, b > 0: a 32-bit division when both fit (the usual case;
+// a 64-bit division is a long instruction sequence)
+__device__ __forceinline__ int64_t udiv64(int64_t a, int64_t b) {
+  if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+  return a / b;
+}
+
+// Pull `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2; no data
+// changes hands and nothing waits for it.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

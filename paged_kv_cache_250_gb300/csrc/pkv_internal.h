@@ -127,7 +127,7 @@ struct DecodeParams {
   int32_t qlen;                // query tokens per sequence (q, out are [B][qlen][Hq][d])
   const void* k_new;           // fused append: new K rows [B][Hkv][d] (NULL: none)
   const void* v_new;           // fused append: new V rows
-  void* k_cache;               // fused append: the caches those rows are written into
+  void* k_cache;               // the caches (pages prefetched into L2; fused append writes)
   void* v_cache;
   int32_t kv_bf16;             // fused append: k_new / v_new are bf16 (else fp16)
   int32_t window;              // > 0: query at position t sees t - window + 1 .. t (and sinks)
