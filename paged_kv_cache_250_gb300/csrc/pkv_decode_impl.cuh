@@ -165,6 +165,10 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
   // the next kernel on the stream may launch (a programmatic dependent waits
   // for this one to complete before it reads what this one writes)
   if (p.trigger_next) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if ((threadIdx.x & 31) == 0) {  // the tensor maps are parameters: fetch them at once
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
   if (!p.early_prologue) griddep_wait();
 
   extern __shared__ uint8_t smem_raw[];
@@ -269,14 +273,24 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
   auto seq_cost0 = [&](int b) -> int64_t {
     return (int64_t)p.Hkv * (pfx[b] + (int64_t)kSegCost * nzp[b]);
   };
-  // first unit whose cost position is >= P (W when none)
+  // Warp-wide search (every lane, the same v): the largest b in [lo, hi)
+  // with key(b) <= v, given key(lo) <= v and key nondecreasing.  Each round
+  // the 32 lanes probe 32 evenly spaced candidates, so 32 sequences take one
+  // round of shared-memory loads and 6000 take three.
+  auto warp_search = [&](auto key, int64_t v, int lo, int hi) -> int {
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) >> 5;
+      const int b = lo + lane * step;
+      const unsigned m = __ballot_sync(0xffffffffu, b < hi && key(b) <= v);
+      lo += (31 - __clz(m)) * step;  // lane 0 probes lo itself: m != 0
+      hi = min(hi, lo + step);
+    }
+    return lo;
+  };
+  // first unit whose cost position is >= P (W when none); every lane, the same P
   auto unit_at_cost = [&](int64_t P) -> int64_t {
     if (P >= Tc) return W;
-    int a = 0, z = p.B;
-    while (z - a > 1) {
-      const int mid = (a + z) >> 1;
-      if (seq_cost0(mid) <= P) a = mid; else z = mid;
-    }
+    const int a = warp_search(seq_cost0, P, 0, p.B);
     const int64_t np = pfx[a + 1] - pfx[a];
     const int64_t r = P - seq_cost0(a);
     const int64_t hh = udiv64(r, np + kSegCost);
@@ -298,6 +312,8 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
     if (s0 >= sh_hi) return make_int2((int)W, (int)W);
     return make_int2((int)s0, (int)(s0 + kRangeMax < sh_hi ? s0 + kRangeMax : sh_hi));
   };
+  // the sequence holding unit x: the last b with Hkv pfx[b] <= x (empty
+  // sequences before it share its pfx); one lane
   auto seq_of = [&](int64_t x) -> int {
     int a = 0, z = p.B;
     while (z - a > 1) {
@@ -399,10 +415,6 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
     return true;
   };
 
-  if (lane == 0) {
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-  }
   const uint64_t pol = l2_policy_evict_first();
 
   // the first piece and its descriptors need nothing the previous kernel
