@@ -87,6 +87,57 @@ def oracle_rows(w: wl.DecodeWorkload, pairs: Iterable[Tuple[int, int]]) -> dict:
     return res
 
 
+def seq_kv_fp64(w: wl.DecodeWorkload, b: int) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 K, V [ctx][Hkv][d] of sequence b (logical_kv_fp64 for every KV
+    head).  16-bit caches widen on the device and copy once."""
+    n = int(w.ctx[b])
+    if not w.cfg.is_fp8:
+        return (w.K_log[b, :n].double().cpu().numpy(), w.V_log[b, :n].double().cpu().numpy())
+    kv = [logical_kv_fp64(w, b, h) for h in range(w.cfg.kv_heads)]
+    return np.stack([k for k, _ in kv], axis=1), np.stack([v for _, v in kv], axis=1)
+
+
+def oracle_whole(w: wl.DecodeWorkload) -> np.ndarray:
+    """Every output row [B][Hq][d]: the oracle's decode_attention (fp64,
+    all host cores) one sequence at a time, so host memory holds one
+    sequence's fp64 cache at most."""
+    cfg = w.cfg
+    q = w.q.double().cpu().numpy()
+    out = np.zeros((cfg.batch, cfg.q_heads, cfg.head_dim))
+    for b in range(cfg.batch):
+        n = int(w.ctx[b])
+        if n == 0:
+            continue  # no rows: the zero output row
+        K, V = seq_kv_fp64(w, b)
+        out[b] = oracle.decode_attention(q[b:b + 1], K[None], V[None], [n],
+                                         cfg.softmax_scale)[0]
+    return out
+
+
+def oracle_multi_seq(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
+                     window: int = 0, sinks: int = 0) -> np.ndarray:
+    """oracle.multi_query_decode (window 0) or oracle.window_decode for every
+    head of one sequence at once: q [QL][Hq][d], K, V [n][Hkv][d] (n >= QL)
+    -> [QL][Hq][d].  Query j sits at position p = n - QL + j and sees the rows
+    t <= p with t > p - window or t < sinks (all t <= p when window is 0);
+    those rows, gathered in order, go through decode_attention."""
+    QL = q.shape[0]
+    n = K.shape[0]
+    assert n >= QL
+    out = np.empty(q.shape)
+    for j in range(QL):
+        p = n - QL + j
+        if window > 0:
+            lo = max(0, p - window + 1)
+            rows = np.concatenate([np.arange(min(sinks, lo)), np.arange(lo, p + 1)])
+            Kj, Vj = K[rows], V[rows]
+        else:
+            Kj, Vj = K[:p + 1], V[:p + 1]
+        out[j] = oracle.decode_attention(q[j][None], Kj[None], Vj[None], [Kj.shape[0]],
+                                         scale)[0]
+    return out
+
+
 def oracle_all(w: wl.DecodeWorkload) -> np.ndarray:
     B, Hq, d = w.cfg.batch, w.cfg.q_heads, w.cfg.head_dim
     out = np.zeros((B, Hq, d))

@@ -13,7 +13,7 @@ import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
 
-from harness import GpuRun, assert_close, oracle_all, oracle_rows
+from harness import oracle_whole, GpuRun, assert_close, oracle_all, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -303,48 +303,24 @@ BENCH_HINT = {"llama3_8b_b32_ctx1-4096_bf16": 4096}
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_configs_sampled(name):
-    cfg = wl.CONFIGS[name]
-    w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
-    out = run.step("bf16" if cfg.cache != "f16" else "f16").double().cpu().numpy()
-    out32 = run.decode("f32").double().cpu().numpy()
-    torch.cuda.synchronize()
-    assert run.err_code() == 0
-    assert np.all(np.isfinite(out32))
-    rng = np.random.default_rng(cfg.seed)
-    ctx = w.ctx.numpy()
-    bs = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), 0, cfg.batch - 1,
-                 *rng.integers(0, cfg.batch, 4).tolist()})
-    pairs = [(b, int(hq)) for b in bs for hq in rng.choice(cfg.q_heads, 3, replace=False)]
-    ref = oracle_rows(w, pairs)
-    r = np.stack([ref[p] for p in pairs])
-    assert_close(np.stack([out32[b, hq] for b, hq in pairs]), r, cfg, "f32", name)
-    assert_close(np.stack([out[b, hq] for b, hq in pairs]), r, cfg,
-                 "bf16" if cfg.cache != "f16" else "f16", name)
-
-
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_timed_step_sampled(name):
-    """Every full-size workload through the call the bench times
-    (pkv_decode_step_fused with PKV_STEP_OVERLAP), sampled rows against the
-    oracle, 16-bit output."""
+def test_full_size_configs_whole(name):
+    """Every full-size workload, every output element against the oracle
+    (fp64, one sequence at a time): the two-call step (16-bit output), the
+    plain decode (fp32 output) and the one-kernel step the bench times
+    (pkv_decode_step_fused with PKV_STEP_OVERLAP, 16-bit output)."""
     cfg = wl.CONFIGS[name]
     w = wl.generate(cfg, device="cuda")
     run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
     odt = "bf16" if cfg.cache != "f16" else "f16"
-    out = run.step_one_kernel(odt, overlap=True).double().cpu().numpy()
+    out = run.step(odt).double().cpu().numpy()
+    out32 = run.decode("f32").double().cpu().numpy()
+    timed = run.step_one_kernel(odt, overlap=True).double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
-    assert np.all(np.isfinite(out))
-    rng = np.random.default_rng(cfg.seed + 17)
-    ctx = w.ctx.numpy()
-    bs = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), cfg.batch - 1,
-                 *rng.integers(0, cfg.batch, 3).tolist()})
-    pairs = [(b, int(hq)) for b in bs for hq in rng.choice(cfg.q_heads, 2, replace=False)]
-    ref = oracle_rows(w, pairs)
-    assert_close(np.stack([out[b, hq] for b, hq in pairs]), np.stack([ref[p] for p in pairs]),
-                 cfg, odt, name)
+    ref = oracle_whole(w)
+    assert_close(out32, ref, cfg, "f32", name)
+    assert_close(out, ref, cfg, odt, name)
+    assert_close(timed, ref, cfg, odt, name + " timed step")
 
 
 @pytest.mark.parametrize("B", [1000, 6000])

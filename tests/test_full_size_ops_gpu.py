@@ -1,7 +1,7 @@
 """The benchmarked forms of the added operations, at their full sizes and in
-the launch configuration the bench times: multi-query decode, the sliding
-window with sinks (sampled rows against the oracle) and whole-block copies
-(every copied byte compared).
+the launch configuration the bench times: multi-query decode and the sliding
+window with sinks (every output element against the oracle, one sequence at
+a time) and whole-block copies (every copied byte compared).
 
 "KV Cache & Flash Attention." (kvcache-7e2.pages.dev): speculative-decoding
 section (several new tokens scored at once), eviction paragraph (a window of
@@ -12,10 +12,9 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, logical_kv_fp64, assert_close
+from harness import GpuRun, assert_close, oracle_multi_seq, seq_kv_fp64
 
 pytestmark = pytest.mark.gpu
 
@@ -50,11 +49,20 @@ def _launch(name, q_len, window=None, sinks=0, seed=0):
     return cfg, w, q, out.double().cpu().numpy()
 
 
-def _sampled_pairs(cfg, w, rng, n_extra=4, heads=2):
-    ctx = w.ctx.numpy()
-    bs = sorted({int(np.argmin(ctx)), int(np.argmax(ctx)), 0, cfg.batch - 1,
-                 *rng.integers(0, cfg.batch, n_extra).tolist()})
-    return [(b, int(hq)) for b in bs for hq in rng.choice(cfg.q_heads, heads, replace=False)]
+def _check_whole(cfg, w, q, got, name, window=0, sinks=0):
+    """Every (sequence, query token, head) row against the oracle; query
+    tokens before position 0 (a context shorter than q_len) get zero rows."""
+    q_len = q.shape[1]
+    qd = q.double().numpy()
+    for b in range(cfg.batch):
+        n = int(w.ctx[b])
+        first = max(0, q_len - n)
+        assert not got[b, :first].any(), f"{name} b{b}: rows before position 0"
+        if first == q_len:
+            continue
+        K, V = seq_kv_fp64(w, b)
+        ref = oracle_multi_seq(qd[b, first:], K, V, cfg.softmax_scale, window, sinks)
+        assert_close(got[b, first:], ref, cfg, "bf16", f"{name} b{b}")
 
 
 @pytest.mark.parametrize("name,q_len", [
@@ -64,18 +72,10 @@ def _sampled_pairs(cfg, w, rng, n_extra=4, heads=2):
     ("llama3_70b_b8_ctx32768_bf16", 4),    # g 8 x 4 tokens: 32 columns over two slices
     ("llama3_8b_b32_ctx1-4096_bf16", 5),   # g 4 x 5 tokens (capacity 8): 32 columns
 ])
-def test_multi_query_full_size_sampled(name, q_len):
+def test_multi_query_full_size_whole(name, q_len):
     cfg, w, q, got = _launch(name, q_len, seed=1)
     assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(cfg.seed + 31)
-    for b, hq in _sampled_pairs(cfg, w, rng):
-        K, V = logical_kv_fp64(w, b, hq // cfg.group)
-        n = K.shape[0]
-        first = max(0, q_len - n)  # tokens before position 0 see nothing
-        if first < q_len:
-            ref = oracle.multi_query_decode(q[b, first:, hq].double().numpy(), K, V,
-                                            cfg.softmax_scale)
-            assert_close(got[b, first:, hq], ref, cfg, "bf16", f"{name} b{b} h{hq}")
+    _check_whole(cfg, w, q, got, name)
 
 
 @pytest.mark.parametrize("name,q_len,window,sinks", [
@@ -83,18 +83,10 @@ def test_multi_query_full_size_sampled(name, q_len):
     ("llama3_8b_b32_ctx1-4096_bf16", 1, 1000, 16),  # windows shorter than many contexts
     ("llama3_70b_b8_ctx32768_bf16", 4, 4096, 4),    # 32 columns under a window
 ])
-def test_window_full_size_sampled(name, q_len, window, sinks):
+def test_window_full_size_whole(name, q_len, window, sinks):
     cfg, w, q, got = _launch(name, q_len, window, sinks, seed=2)
     assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(cfg.seed + 37)
-    for b, hq in _sampled_pairs(cfg, w, rng):
-        K, V = logical_kv_fp64(w, b, hq // cfg.group)
-        n = K.shape[0]
-        first = max(0, q_len - n)
-        if first < q_len:
-            ref = oracle.window_decode(q[b, first:, hq].double().numpy(), K, V,
-                                       cfg.softmax_scale, window, sinks)
-            assert_close(got[b, first:, hq], ref, cfg, "bf16", f"{name} b{b} h{hq}")
+    _check_whole(cfg, w, q, got, name, window, sinks)
 
 
 def test_copy_blocks_full_size_bit_exact():

@@ -12,7 +12,8 @@ import torch
 import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, logical_kv_fp64, assert_close, assert_same_rounding
+from harness import (GpuRun, assert_close, assert_same_rounding, logical_kv_fp64,
+                     oracle_multi_seq, seq_kv_fp64)
 
 PAGE = wl.PAGE
 
@@ -128,23 +129,19 @@ def test_window_covering_everything_equals_plain_decode(window, sinks):
 
 
 @pytest.mark.gpu
-def test_window_full_size_sampled():
-    """A long-context batch under a 4096-token window: sampled (sequence,
-    head) rows against the oracle, in the launch the bench times."""
+def test_window_long_contexts_whole():
+    """A long-context batch under a 4096-token window, in the launch the
+    bench times: every output row against the oracle."""
     window, sinks = 4096, 4
     cfg, w, run = _setup("long", 8, 32, 8, 128, "bf16",
                          [16384, 9000, 4097, 4096, 12345, 70, 8191, 16000], 54)
     q = _q(cfg, 1, 4)
     got = _window_call(run, cfg, q, window, sinks).cpu().double().numpy()
-    rng = np.random.default_rng(5)
+    qd = q.double().numpy()
     for b in range(cfg.batch):
-        h = int(rng.integers(cfg.kv_heads))
-        K, V = logical_kv_fp64(w, b, h)
-        for hh in range(cfg.group):
-            hq = h * cfg.group + hh
-            ref = oracle.window_decode(q[b, :, hq].double().numpy(), K, V, cfg.softmax_scale,
-                                       window, sinks)
-            assert_close(got[b, :, hq], ref, cfg, "f32", f"long b{b} h{hq}")
+        K, V = seq_kv_fp64(w, b)
+        ref = oracle_multi_seq(qd[b], K, V, cfg.softmax_scale, window, sinks)
+        assert_close(got[b], ref, cfg, "f32", f"long b{b}")
 
 
 @pytest.mark.gpu
