@@ -1032,7 +1032,8 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
   // the NW states and writes) rotates from flush to flush.
   // Synchronous form (used when the other warps' compact states do not fit
   // in mbuf): a tree of CTA barriers over two state buffers; each round the
-  // two highest roles left hand their states to roles 0 and 1.
+  // m highest of the n roles left (m = 2, or 1 when n is 3) hand their states
+  // to roles 0 .. m - 1, until roles 0 and 1 are left.
   auto flush_sync = [&](int b, int h, bool split, int pages_mine) {
     float* buf0 = mbuf;
     float* buf1 = mbuf + C::kLaneState * 32;
@@ -1042,10 +1043,11 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
     merge_barrier();
     merge_flagged();  // uses mbuf, before the states go there
 #pragma unroll
-    for (int n = NW; n > 2; n -= 2) {
-      if (wr >= n - 2 && wr < n) store_state(wr == n - 2 ? buf0 : buf1);
+    for (int n = NW; n > 2; n -= (n >= 4 ? 2 : 1)) {
+      const int m = n >= 4 ? 2 : 1;
+      if (wr >= n - m && wr < n) store_state(wr == n - m ? buf0 : buf1);
       merge_barrier();
-      if (wr < 2) merge_state(wr == 0 ? buf0 : buf1);
+      if (wr < m) merge_state(wr == 0 ? buf0 : buf1);
       merge_barrier();
     }
     if (wr == 1) store_state(buf0);
