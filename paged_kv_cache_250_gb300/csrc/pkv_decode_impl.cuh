@@ -80,7 +80,7 @@ struct Int {  // a compile-time count passed to a generic lambda
   static constexpr int value = N;
 };
 
-template <int D, int CACHE>
+template <int D, int CACHE, bool DEEP = false>
 struct DecodeCfg {
   static constexpr int kElem = cache_is_fp8((CacheKind)CACHE) ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;              // bytes per token row
@@ -91,7 +91,8 @@ struct DecodeCfg {
   static constexpr int kScaleBytes = decode_scale_bytes((CacheKind)CACHE);  // per stage
   static constexpr int kKSteps = D / 16;  // k-steps of the QK contraction
   static constexpr int kMTiles = D / 16;  // 16-row tiles of O^T
-  static constexpr int kStages = decode_stages(D, (CacheKind)CACHE);
+  static constexpr int kStages =
+      DEEP ? decode_stages_deep(D, (CacheKind)CACHE) : decode_stages(D, (CacheKind)CACHE);
   static constexpr int kLaneState = 4 + 4 * kMTiles;  // m[2], l[2], o[MT][4] per lane
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte boxes");
 };
@@ -137,20 +138,21 @@ __device__ __forceinline__ void store_out_rt(pkv_dtype t, void* base, int64_t id
 // sequence the kernel is built for (p.qlen <= QC of them are real).  The
 // MMA's 8 columns hold the NC = QC * G (query token, head) pairs of a group.
 // The library builds it for one query token (QC = 1); several query tokens
-// per sequence go to the kernel of pkv_decode_mq.cuh.
-template <int D, int G, int QC, int CACHE, bool QBF16>
+// per sequence go to the kernel of pkv_decode_mq.cuh.  DEEP: the deeper ring
+// and barrier-tree segment ends of the per-token E4M3 kernel at small batches.
+template <int D, int G, int QC, int CACHE, bool QBF16, bool DEEP>
 __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCtasPerSm)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
   constexpr int NC = G * QC;
   static_assert(NC <= 8, "one MMA column per (query token, head)");
-  using C = DecodeCfg<D, CACHE>;
+  using C = DecodeCfg<D, CACHE, DEEP>;
   constexpr bool kBF = (CACHE == kCacheBF16);  // mma operand type (else fp16)
   constexpr int kS = C::kStages;
   constexpr int NW = decode_warps((CacheKind)CACHE);
   constexpr int kDescRing = decode_desc_ring(NW);  // page descriptors per warp
   static_assert(2 * ((kRangeMax + NW - 1) / NW) <= kDescRing, "two pieces per ring");
-  constexpr int kMbuf = decode_mbuf_floats(D, NW);
+  constexpr int kMbuf = DEEP ? 2 * C::kLaneState * 32 : decode_mbuf_floats(D, NW);
   auto merge_barrier = [] { pkv::merge_barrier<NW>(); };
   constexpr int kMT = C::kMTiles;
   // pages a warp takes per step: 2 on rings of 3+ pages (4 measured slower:
@@ -1071,7 +1073,7 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
   // waited for by the warps whose arrivals complete phase n - 1.
   constexpr int kU = NC >= 4 ? NC / 2 : 1;     // C-fragment column pairs with real columns
   constexpr int kCS = C::kLaneState * 8 * kU;  // floats per compact warp state
-  constexpr bool kAsyncFlush = NC <= 4 && (NW - 1) * kCS <= kMbuf;
+  constexpr bool kAsyncFlush = !DEEP && NC <= 4 && (NW - 1) * kCS <= kMbuf;
   auto flush_async = [&](int b, int h, bool split, int pages_mine) {
     const int n = nflushes++;
     const int fin = n % NW;
@@ -1226,10 +1228,10 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
 
 // ---------------------------------------------------------------------------
 // Host-side dispatch over head_dim, group and query tokens for one cache kind.
-template <int D, int G, int QC, int CACHE, bool QBF16>
+template <int D, int G, int QC, int CACHE, bool QBF16, bool DEEP>
 cudaError_t launch_split(const DecodeLaunch& l) {
-  auto kern = decode_kernel<D, G, QC, CACHE, QBF16>;
-  const size_t smem = decode_smem_bytes(D, (CacheKind)CACHE, l.p.B);
+  auto kern = decode_kernel<D, G, QC, CACHE, QBF16, DEEP>;
+  const size_t smem = decode_smem_bytes_form(D, (CacheKind)CACHE, l.p.B, DEEP);
   static size_t configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1255,8 +1257,13 @@ template <int CACHE, bool QBF16>
 cudaError_t dispatch_split(const DecodeLaunch& l) {
   const int d = l.p.d;
   const int g = l.group;
-#define PKV_CASE(DD, GG) \
-  if (d == DD && g == GG) return launch_split<DD, GG, 1, CACHE, QBF16>(l);
+  const bool deep = decode_use_deep(d, (CacheKind)CACHE, l.p.B);
+#define PKV_CASE(DD, GG)                                                         \
+  if (d == DD && g == GG) {                                                      \
+    if constexpr (CACHE == kCacheE4M3Tok)                                        \
+      if (deep) return launch_split<DD, GG, 1, CACHE, QBF16, true>(l);           \
+    return launch_split<DD, GG, 1, CACHE, QBF16, false>(l);                      \
+  }
   if constexpr (!cache_is_fp8((CacheKind)CACHE)) {
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
   }

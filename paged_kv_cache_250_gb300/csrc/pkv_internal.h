@@ -168,11 +168,33 @@ struct AppendParams {
 
 // Dynamic shared memory the single-token kernel needs for a batch of B
 // sequences.
-inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
-  return (size_t)decode_fixed_smem(d, cache) +
-         (size_t)decode_warps(cache) * decode_stages(d, cache) *
+// The "deep" form of the per-token E4M3 kernel: its segment ends go through
+// the barrier tree (two whole warp states in the merge buffer instead of the
+// others' compact states), which leaves room for one more page slot per warp
+// (four instead of three) when the batch's per-sequence arrays are small
+// (up to about 100 sequences at d 128).
+__host__ __device__ constexpr int decode_fixed_smem_deep(int d, CacheKind c) {
+  return 1024 + decode_warps(c) * decode_desc_ring(decode_warps(c)) * 8 +
+         2 * decode_lane_state(d) * 32 * 4 + 2 * decode_warps(c) * 4 + decode_warps(c) * 8 * 8 +
+         32;
+}
+__host__ __device__ constexpr int decode_stages_deep(int d, CacheKind c) {
+  return decode_clamp_stages((kDecodeSmemTarget - decode_fixed_smem_deep(d, c)) /
+                             (decode_warps(c) * (decode_stage_bytes(d, c) + decode_scale_bytes(c))));
+}
+inline size_t decode_smem_bytes_form(int32_t d, CacheKind cache, int32_t B, bool deep) {
+  return (size_t)(deep ? decode_fixed_smem_deep(d, cache) : decode_fixed_smem(d, cache)) +
+         (size_t)decode_warps(cache) * (deep ? decode_stages_deep(d, cache) : decode_stages(d, cache)) *
              (decode_stage_bytes(d, cache) + decode_scale_bytes(cache)) +
          (size_t)(5 * B + 2) * 4;
+}
+// whether a single-token launch of B sequences takes the deep form
+inline bool decode_use_deep(int32_t d, CacheKind cache, int32_t B) {
+  return cache == kCacheE4M3Tok && decode_stages_deep(d, cache) > decode_stages(d, cache) &&
+         decode_smem_bytes_form(d, cache, B, true) <= (size_t)kDecodeSmemTarget;
+}
+inline size_t decode_smem_bytes(int32_t d, CacheKind cache, int32_t B) {
+  return decode_smem_bytes_form(d, cache, B, decode_use_deep(d, cache, B));
 }
 // The same for the multi-query kernel built for nc columns.
 inline size_t mq_smem_bytes(int32_t d, CacheKind cache, int32_t B, int32_t nc) {

@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, assert_close, oracle_all, oracle_rows
+from harness import GpuRun, assert_close, oracle_all, oracle_rows, oracle_whole
 
 pytestmark = pytest.mark.gpu
 
@@ -70,6 +70,25 @@ def test_decode_matches_the_oracle(g, q_dtype):
     err = assert_close(out, ref, cfg, "f32", "per-token fp32 out")
     assert err < 2e-3  # the expected error is far inside the 3e-2 gate
     assert_close(out_bf, ref, cfg, "bf16", "per-token bf16 out")
+
+
+@pytest.mark.parametrize("B", [104, 105, 300])
+def test_both_ring_depths_match_the_oracle(B):
+    """Batches on both sides of the size where the per-token kernel's deeper
+    ring (four page slots per warp, barrier-tree segment ends) stops fitting
+    two CTAs per SM and the three-slot form with the asynchronous hand-off
+    runs instead: every output row against the oracle, with many short
+    sequences (so many segment ends) and some long ones (split segments)."""
+    gen = torch.Generator().manual_seed(B)
+    ctx = torch.randint(0, 48, (B,), generator=gen, dtype=torch.int32)
+    ctx[::37] = 700
+    cfg = wl.small_config(f"tok_depth_{B}", B, 32, 8, 128, "e4m3tok", 1, seed=93)
+    w = wl.generate(cfg, ctx_override=ctx)
+    run = GpuRun(w)
+    out = run.step("f32").double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert run.err_code() == 0
+    assert_close(out, oracle_whole(w), cfg, "f32", f"per-token B {B}")
 
 
 def test_one_kernel_step_equals_two_kernel_step():
