@@ -352,8 +352,7 @@ PKV_API pkv_status pkv_decode_step_fused(
  *     checked before anything is put on the stream.
  *   - The first call on each device looks up the scratch array's device
  *     address (cudaGetSymbolAddress) and keeps it for the life of the
- *     process; make that first call before any stream capture on that
- *     device.  The kept address belongs to the device's primary context (the
+ *     process.  The kept address belongs to the device's primary context (the
  *     one the CUDA runtime uses): calls from another context on the device,
  *     or after a cudaDeviceReset, are not supported.
  *   - Every call on a device shares the one array and leaves its contents
