@@ -120,7 +120,8 @@ WsLayout ws_layout(const pkv_cache_desc* d, int32_t batch, int32_t mbs, int32_t 
   const int64_t np_max = (len + kPageSize - 1) / kPageSize;
   const int64_t segs = (int64_t)batch * d->num_kv_heads;
   const int64_t pages_bound = segs * np_max;
-  // at least two pages per warp; at most kDecodeCtasPerSm CTAs per SM
+  // at least eight pages per CTA (two per warp of a four-warp CTA); at most
+  // kDecodeCtasPerSm CTAs per SM
   int64_t ctas = (pages_bound + 2 * pkv::kDecodeWarps - 1) / (2 * pkv::kDecodeWarps);
   const int64_t max_ctas = (int64_t)num_sms * pkv::kDecodeCtasPerSm;
   if (ctas > max_ctas) ctas = max_ctas;

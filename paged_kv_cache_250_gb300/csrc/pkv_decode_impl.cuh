@@ -853,9 +853,10 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
 
   // ---- merging the partials of a completed segment.  Threads t, t+T, ...
   // (T threads: one warp mid-kernel, the whole CTA at exit) take float4
-  // columns t, t+T, ...; each column finds its head's common maximum M over
-  // the partials, then adds them in slot order, so the result is bitwise the
-  // same whichever form runs.  No shared memory, no barrier.
+  // columns t, t+T, ...; each column adds its head's partials in slot order
+  // (against a running maximum for up to four partials, else against their
+  // common maximum), so the result is bitwise the same whichever form runs.
+  // No shared memory, no barrier.
   auto merge_cols = [&](int seg, int t, int T) {
     const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
     const int64_t np = pfx[b + 1] - pfx[b];
@@ -870,25 +871,56 @@ __global__ void __launch_bounds__(decode_warps((CacheKind)CACHE) * 32, kDecodeCt
       if (!col_real(head)) continue;
       const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + slot_base * NC + head;
       const float4* vo = reinterpret_cast<const float4*>(p.part_o + slot_base * NC * D) + col;
-      float M = -INFINITY;
-#pragma unroll 4
-      for (int kk = 0; kk < count; ++kk) {
-        const float2 v = __ldcg(ml + (int64_t)kk * NC);
-        if (v.y > 0.f) M = fmaxf(M, v.x);
-      }
+      float M = -INFINITY, lsum = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float lsum = 0.f;
-      if (M > -INFINITY) {
+      if (count <= 4) {
+        // a few partials: one pass in slot order, the running reference
+        // moving up to each new maximum and what was summed brought down to
+        // it, so all their loads go out at once
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (kk < count) {
+            const float2 v = __ldcg(ml + (int64_t)kk * NC);
+            const float4 x = __ldcg(vo + (int64_t)kk * (NC * D / 4));
+            if (v.y > 0.f) {
+              if (v.x > M) {
+                const float a = exp2f(M - v.x);  // 0 while nothing is summed
+                lsum *= a;
+                acc.x *= a;
+                acc.y *= a;
+                acc.z *= a;
+                acc.w *= a;
+                M = v.x;
+              }
+              const float w = exp2f(v.x - M);
+              lsum += w * v.y;
+              acc.x += w * x.x;
+              acc.y += w * x.y;
+              acc.z += w * x.z;
+              acc.w += w * x.w;
+            }
+          }
+        }
+      } else {
+        // many: the common maximum first, then the weighted sum (the
+        // exponentials independent of one another)
 #pragma unroll 4
         for (int kk = 0; kk < count; ++kk) {
           const float2 v = __ldcg(ml + (int64_t)kk * NC);
-          const float4 x = __ldcg(vo + (int64_t)kk * (NC * D / 4));
-          const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
-          lsum += w * v.y;
-          acc.x += w * x.x;
-          acc.y += w * x.y;
-          acc.z += w * x.z;
-          acc.w += w * x.w;
+          if (v.y > 0.f) M = fmaxf(M, v.x);
+        }
+        if (M > -INFINITY) {
+#pragma unroll 4
+          for (int kk = 0; kk < count; ++kk) {
+            const float2 v = __ldcg(ml + (int64_t)kk * NC);
+            const float4 x = __ldcg(vo + (int64_t)kk * (NC * D / 4));
+            const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+            lsum += w * v.y;
+            acc.x += w * x.x;
+            acc.y += w * x.y;
+            acc.z += w * x.z;
+            acc.w += w * x.w;
+          }
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
