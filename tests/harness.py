@@ -148,7 +148,7 @@ def oracle_all(w: wl.DecodeWorkload) -> np.ndarray:
 
 
 # ------------------------------------------------------------------ CUDA side
-class GpuRun:
+class DeviceRun:
     """Device copies of a workload and one append + decode through the C ABI."""
 
     def __init__(self, w: wl.DecodeWorkload, device="cuda", hint: int = 0,

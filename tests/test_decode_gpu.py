@@ -13,7 +13,7 @@ import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
 
-from harness import oracle_whole, GpuRun, assert_close, oracle_all, oracle_rows
+from harness import oracle_whole, DeviceRun, assert_close, oracle_all, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,7 @@ RAGGED = [1, 2, 15, 16, 17, 31, 33, 250, 600, 1000]
 def test_tiny_decode_step(ctx, out_dtype):
     cfg = wl.CONFIGS["tiny_b1_h4x1_d64_f16_ctx256"]
     w = wl.generate(cfg, ctx_override=torch.tensor([ctx]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step(out_dtype).double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
@@ -48,7 +48,7 @@ def test_ragged_sweep_16bit(cache, d, g, fused):
     cfg = wl.small_config(f"sweep_{cache}_{d}_{g}", len(RAGGED), 2 * g, 2, d, cache, 1,
                           seed=11 + g + d)
     w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out32 = run.step("f32", fused=fused).double().cpu().numpy()
     out16 = run.decode(cache).double().cpu().numpy()
     torch.cuda.synchronize()
@@ -64,7 +64,7 @@ def test_ragged_sweep_fp8(g, q_dtype):
     cfg = wl.small_config(f"sweep_fp8_{g}", len(RAGGED), 2 * g, 2, 128, "e4m3", 1,
                           seed=23 + g, q_dtype=q_dtype)
     w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     out_bf = run.decode("bf16").double().cpu().numpy()
     torch.cuda.synchronize()
@@ -89,7 +89,7 @@ def test_fp8_bf16_q_outside_fp16_range(cache, mag):
     w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
     w.q = (w.q.float() * mag).to(torch.bfloat16)  # the oracle reads the same bf16 q
     assert float(w.q.float().abs().max()) > 65504.0 or float(w.q.float().abs().max()) < 6e-5
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
@@ -102,7 +102,7 @@ def test_many_splits_long_sequence():
     # one long sequence spread over every warp of the grid, plus short ones
     cfg = wl.small_config("long", 3, 8, 2, 128, "bf16", 1, seed=5)
     w = wl.generate(cfg, ctx_override=torch.tensor([20000, 3, 4097]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     torch.cuda.synchronize()
     ref = oracle_all(w)
@@ -114,7 +114,7 @@ def test_many_splits_long_sequence():
 def test_append_is_bit_exact(cache):
     cfg = wl.small_config("append", 6, 8, 2, 128, cache, 1, seed=3)
     w = wl.generate(cfg, ctx_override=torch.tensor([1, 16, 17, 100, 5, 64]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     torch.cuda.synchronize()
     view = torch.int16
@@ -168,7 +168,7 @@ def test_append_skips_negative_slots_and_reports_out_of_pool():
     slot[0] = -1
     slot[2] = w.num_blocks * 16 + 3  # past the pool
     w.slot_mapping = slot
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     torch.cuda.synchronize()
     view = torch.int16
@@ -188,7 +188,7 @@ def test_paging_is_invisible_to_the_result():
         cfg = wl.DecodeConfig("inv", 5, 8, 2, 128, "bf16", 1, table=table, seed=9,
                               spare_blocks=7)
         w = wl.generate(cfg, ctx_override=ctx)
-        run = GpuRun(w)
+        run = DeviceRun(w)
         outs.append(run.step("f32").cpu())
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
@@ -197,7 +197,7 @@ def test_paging_is_invisible_to_the_result():
 def test_repeatable_and_zero_context_rows():
     cfg = wl.small_config("zero", 5, 8, 2, 128, "bf16", 1, seed=4)
     w = wl.generate(cfg, ctx_override=torch.tensor([0, 33, 0, 1, 5000]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     a = run.decode("f32").cpu()
     b = run.decode("f32").cpu()
@@ -206,14 +206,14 @@ def test_repeatable_and_zero_context_rows():
     ref = oracle_all(w)
     assert_close(a.double().numpy(), ref, cfg, "f32", "zero-ctx batch")
     allzero = wl.generate(cfg, ctx_override=torch.tensor([0, 0, 0, 0, 0]))
-    run0 = GpuRun(allzero)
+    run0 = DeviceRun(allzero)
     assert torch.all(run0.decode("bf16") == 0)
 
 
 def test_long_ragged_batch_is_repeatable_and_matches_the_oracle():
     cfg = wl.small_config("det", 7, 32, 8, 128, "bf16", (1, 6000), seed=17)
     w = wl.generate(cfg)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     # which CTA merges a split segment, and when, depends on timing; the
     # result must not
@@ -229,8 +229,8 @@ def test_one_workspace_across_workloads_of_different_sizes():
     big = wl.small_config("big", 9, 32, 8, 128, "bf16", (200, 3000), seed=23)
     small = wl.small_config("small", 3, 32, 8, 128, "bf16", (1, 40), seed=24)
     wb, ws = wl.generate(big), wl.generate(small)
-    rb = GpuRun(wb)
-    rs = GpuRun(ws)
+    rb = DeviceRun(wb)
+    rs = DeviceRun(ws)
     rs.workspace = rb.workspace  # shared; the big workload's size covers both
     refb, refs = oracle_all(wb), oracle_all(ws)
     rb.step("f32")
@@ -251,7 +251,7 @@ def test_prefix_sharing_tables():
     # the logical view of sequence 1 now starts with sequence 0's tokens
     w.K_log[1, :48] = w.K_log[0, :48]
     w.V_log[1, :48] = w.V_log[0, :48]
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     torch.cuda.synchronize()
     ref = oracle_all(w)
@@ -264,7 +264,7 @@ def test_bad_block_table_entry_is_reported_not_read():
     tables = w.block_tables.clone()
     tables[1, 1] = w.num_blocks + 100
     w.block_tables = tables
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == pkv.PKV_ERR_BOUNDS
@@ -277,7 +277,7 @@ def test_bad_block_table_entry_is_reported_not_read():
 def test_host_side_argument_errors():
     cfg = wl.small_config("args", 2, 8, 2, 128, "bf16", 1, seed=1)
     w = wl.generate(cfg, ctx_override=torch.tensor([5, 6]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = torch.empty(2, 8, 128, dtype=torch.float32, device="cuda")
     small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(pkv.PkvError) as e:
@@ -310,7 +310,7 @@ def test_full_size_configs_whole(name):
     (pkv_decode_step_fused with PKV_STEP_OVERLAP, 16-bit output)."""
     cfg = wl.CONFIGS[name]
     w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
+    run = DeviceRun(w, hint=BENCH_HINT.get(name, 0))
     odt = "bf16" if cfg.cache != "f16" else "f16"
     out = run.step(odt).double().cpu().numpy()
     out32 = run.decode("f32").double().cpu().numpy()
@@ -331,7 +331,7 @@ def test_large_batches_of_short_contexts(B):
     against the oracle, empty sequences exactly zero."""
     cfg = wl.small_config(f"big_{B}", B, 32, 8, 128, "bf16", (0, 40), seed=31)
     w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step_one_kernel("f32", overlap=True)
     torch.cuda.synchronize()
     assert run.err_code() == 0

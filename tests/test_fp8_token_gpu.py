@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, assert_close, oracle_all, oracle_rows, oracle_whole
+from harness import DeviceRun, assert_close, oracle_all, oracle_rows, oracle_whole
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,7 @@ def test_decode_matches_the_oracle(g, q_dtype):
     cfg = wl.small_config(f"tok_{g}", len(RAGGED), 2 * g, 2, 128, "e4m3tok", 1, seed=92 + g,
                           q_dtype=q_dtype)
     w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     out_bf = run.decode("bf16").double().cpu().numpy()
     torch.cuda.synchronize()
@@ -84,7 +84,7 @@ def test_both_ring_depths_match_the_oracle(B):
     ctx[::37] = 700
     cfg = wl.small_config(f"tok_depth_{B}", B, 32, 8, 128, "e4m3tok", 1, seed=93)
     w = wl.generate(cfg, ctx_override=ctx)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
@@ -94,7 +94,7 @@ def test_both_ring_depths_match_the_oracle(B):
 def test_one_kernel_step_equals_two_kernel_step():
     cfg = wl.small_config("tok_step", len(RAGGED), 8, 2, 128, "e4m3tok", 1, seed=97)
     w = wl.generate(cfg, ctx_override=torch.tensor(RAGGED))
-    one, two = GpuRun(w), GpuRun(w)
+    one, two = DeviceRun(w), DeviceRun(w)
     o1 = one.step_one_kernel("f32")
     o2 = two.step("f32", fused=True)
     torch.cuda.synchronize()
@@ -110,7 +110,7 @@ def test_long_sequence_and_window():
     per-token cache, against the oracle."""
     cfg = wl.small_config("tok_long", 3, 8, 2, 128, "e4m3tok", 1, seed=98)
     w = wl.generate(cfg, ctx_override=torch.tensor([20000, 5, 3000]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = run.step("f32").double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
@@ -136,7 +136,7 @@ def test_long_sequence_and_window():
 def test_copy_blocks_moves_the_scales():
     cfg = wl.small_config("tok_cow", 2, 8, 2, 128, "e4m3tok", 1, seed=99)
     w = wl.generate(cfg, ctx_override=torch.tensor([40, 20]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     tab = w.block_tables
     src = torch.tensor([int(tab[0, 0]), int(tab[0, 2])], dtype=torch.int32)
     dst = torch.tensor([int(tab[1, 0]), w.num_blocks - 1], dtype=torch.int32)
@@ -154,7 +154,7 @@ def test_multi_query_matches_the_oracle(g, q_len):
     per-token cache."""
     cfg = wl.small_config(f"tok_mq_{g}", 4, 2 * g, 2, 128, "e4m3tok", 1, seed=100 + g)
     w = wl.generate(cfg, ctx_override=torch.tensor([1, 9, 300, 1200]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     gq = torch.Generator().manual_seed(7 + g)
     q = torch.randn(4, q_len, cfg.q_heads, 128, generator=gq).to(cfg.qdt)

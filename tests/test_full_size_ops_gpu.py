@@ -14,7 +14,7 @@ import torch
 
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, assert_close, oracle_multi_seq, seq_kv_fp64
+from harness import DeviceRun, assert_close, oracle_multi_seq, seq_kv_fp64
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,7 @@ def _launch(name, q_len, window=None, sinks=0, seed=0):
     with the bench's bf16 output, after the append of the newest token."""
     cfg = wl.CONFIGS[name]
     w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w, hint=BENCH_HINT.get(name, 0))
+    run = DeviceRun(w, hint=BENCH_HINT.get(name, 0))
     run.append()
     # the bench's workspace: partials of group x q_len columns
     n = pkv.pkv_decode_workspace_bytes_multi(run.desc, cfg.batch, q_len, w.max_blocks_per_seq,

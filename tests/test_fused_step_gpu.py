@@ -11,7 +11,7 @@ import torch
 
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, assert_close, oracle_all, oracle_rows, oracle_whole
+from harness import DeviceRun, assert_close, oracle_all, oracle_rows, oracle_whole
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def _bytes(t: torch.Tensor) -> torch.Tensor:
 def _both_ways(w, out_dtype="f32"):
     """Run the one-kernel step and the two-kernel step on separate copies of
     the same inputs; return both outputs and both runs."""
-    one, two = GpuRun(w), GpuRun(w)
+    one, two = DeviceRun(w), DeviceRun(w)
     out1 = one.step_one_kernel(out_dtype)
     out2 = two.step(out_dtype, fused=True)
     torch.cuda.synchronize()
@@ -67,7 +67,7 @@ def test_one_kernel_step_empty_and_single_token_sequences():
     token alone, so the output is its V row exactly."""
     cfg = wl.small_config("one_edge", 4, 8, 2, 128, "bf16", 1, seed=81)
     w = wl.generate(cfg, ctx_override=torch.tensor([0, 1, 17, 0]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     before_k, before_v = _bytes(run.k_cache).clone(), _bytes(run.v_cache).clone()
     out = run.step_one_kernel("f32")
     torch.cuda.synchronize()
@@ -106,7 +106,7 @@ def test_one_kernel_step_full_size_whole():
     checked whole with the other full-size configs)."""
     cfg = wl.CONFIGS["llama3_8b_b32_ctx1-4096_bf16"]
     w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w, hint=4096)
+    run = DeviceRun(w, hint=4096)
     out = run.step_one_kernel("bf16", overlap=False).double().cpu().numpy()
     torch.cuda.synchronize()
     assert run.err_code() == 0
@@ -127,7 +127,7 @@ def test_overlapped_steps_chain(cache):
     prev = (ctx - 2).clamp(min=0)
     runs = []
     for overlap in (True, False):
-        run = GpuRun(w)
+        run = DeviceRun(w)
         tab = run.tables.to(torch.int64)
         ar = torch.arange(cfg.batch, device="cuda")
         pos = prev.cuda()
@@ -167,7 +167,7 @@ def test_overlapped_steps_chain(cache):
 def test_one_kernel_step_argument_errors():
     cfg = wl.small_config("one_args", 2, 8, 2, 128, "bf16", 1, seed=83)
     w = wl.generate(cfg, ctx_override=torch.tensor([5, 9]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     out = torch.empty(2, 8, 128, dtype=torch.float32, device="cuda")
     with pytest.raises(pkv.PkvError):  # 16-bit cache: new rows must match its dtype
         pkv.pkv_decode_step_fused(run.desc, run.q, run.k_cache, run.v_cache,

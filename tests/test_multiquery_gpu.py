@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, logical_kv_fp64, assert_close, assert_same_rounding
+from harness import DeviceRun, logical_kv_fp64, assert_close, assert_same_rounding
 
 _DT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
@@ -25,7 +25,7 @@ def multi_workspace(run, cfg, q_len):
 
 def _run(cfg, ctx, q_len, out_dtype="f32", seed=0):
     w = wl.generate(cfg, ctx_override=torch.tensor(ctx))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()  # the newest token; the other new tokens are already cached
     run.workspace = multi_workspace(run, cfg, q_len)
     qdt = cfg.qdt
@@ -94,7 +94,7 @@ def test_multi_query_matches_the_oracle(case):
 def test_multi_query_one_token_equals_single_decode():
     cfg = wl.small_config("q1", 4, 8, 2, 128, "bf16", (1, 900), seed=42)
     w = wl.generate(cfg)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     single = run.decode("f32")
     out = torch.empty(cfg.batch, 1, cfg.q_heads, cfg.head_dim, dtype=torch.float32, device="cuda")
@@ -110,7 +110,7 @@ def test_multi_query_one_token_equals_single_decode():
 def test_multi_query_rejects_too_many_tokens():
     cfg = wl.small_config("big_q", 2, 8, 2, 128, "bf16", 64, seed=43)
     w = wl.generate(cfg)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     q = torch.zeros(2, 9, 8, 128, dtype=torch.bfloat16, device="cuda")  # 9 query tokens
     out = torch.empty_like(q)
     with pytest.raises(pkv.PkvError) as e:

@@ -12,7 +12,7 @@ import torch
 import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import GpuRun, logical_kv_fp64, assert_close, seq_kv_fp64
+from harness import DeviceRun, logical_kv_fp64, assert_close, seq_kv_fp64
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +22,7 @@ _DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 def _setup(name, Hq, Hkv, cache, ctx, seed, d=128):
     cfg = wl.small_config(name, len(ctx), Hq, Hkv, d, cache, 1, seed=seed)
     w = wl.generate(cfg, ctx_override=torch.tensor(ctx))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()  # every position of every sequence is now in the cache
     return cfg, w, run
 
@@ -127,7 +127,7 @@ def test_prefill_bad_rows_are_reported_not_computed():
 def test_prefill_unsupported_shapes():
     cfg = wl.small_config("fp8", 2, 8, 2, 128, "e4m3", 1, seed=65)
     w = wl.generate(cfg, ctx_override=torch.tensor([10, 20]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     q = torch.zeros(4, 8, 128, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(4, 8, 128, dtype=torch.float32, device="cuda")
     starts = torch.tensor([0, 2, 4], dtype=torch.int32, device="cuda")
@@ -143,7 +143,7 @@ def test_prefill_full_size_sampled():
     against the oracle's attention over exactly the positions each row sees."""
     cfg = wl.CONFIGS["llama3_8b_b8_ctx8192_bf16"]
     w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     chunk = 2048
     q, starts, out = _prefill(run, cfg, [chunk] * cfg.batch, "bf16", seed=5)

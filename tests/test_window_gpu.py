@@ -12,7 +12,7 @@ import torch
 import oracle
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
-from harness import (GpuRun, assert_close, assert_same_rounding, logical_kv_fp64,
+from harness import (DeviceRun, assert_close, assert_same_rounding, logical_kv_fp64,
                      oracle_multi_seq, seq_kv_fp64)
 
 PAGE = wl.PAGE
@@ -57,7 +57,7 @@ def _oracle(w, cfg, q, window, sinks):
 def _setup(name, B, Hq, Hkv, d, cache, ctx, seed):
     cfg = wl.small_config(name, B, Hq, Hkv, d, cache, 1, seed=seed)
     w = wl.generate(cfg, ctx_override=torch.tensor(ctx))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     return cfg, w, run
 

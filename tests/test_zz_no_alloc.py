@@ -15,7 +15,7 @@ import torch
 import paged_kv_cache_250_gb300 as pkv
 from paged_kv_cache_250_gb300 import workloads as wl
 
-from harness import GpuRun, assert_close, oracle_all
+from harness import DeviceRun, assert_close, oracle_all
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 def test_noalloc_matches_regular_entry_point_twice_in_a_row():
     cfg = wl.small_config("noalloc", 6, 16, 4, 128, "bf16", 1, seed=21)
     w = wl.generate(cfg, ctx_override=torch.tensor([1, 17, 300, 64, 1000, 33]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     ref = run.decode("f32")  # regular entry point with a caller workspace
     outs = []
@@ -68,7 +68,7 @@ def test_noalloc_on_a_side_stream_and_argument_errors_first():
     # point.  An invalid argument is refused before anything is queued.
     cfg = wl.small_config("noalloc_stream", 5, 8, 2, 128, "bf16", 1, seed=22)
     w = wl.generate(cfg, ctx_override=torch.tensor([3, 700, 40, 1, 2048]))
-    run = GpuRun(w)
+    run = DeviceRun(w)
     run.append()
     ref = run.decode("f32")
     torch.cuda.synchronize()
