@@ -465,7 +465,9 @@ def run_native(args, cfg, rank, world, device):
                           "device-to-host copy of the output; double-buffered, the copies on their "
                           "own streams overlapping the neighbouring steps; all inside the timed "
                           "graph; median of three replays of the K-step graph"},
-        "gpu_launches": K,
+        # the one-kernel step is one launch for 16-bit caches; E4M3 steps
+        # enqueue the append kernel, then the attention
+        "gpu_launches": K * (2 if cfg.is_fp8 else 1),
         "clocks": clocks,
     }
     return res, st
