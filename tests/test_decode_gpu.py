@@ -323,13 +323,14 @@ def test_full_size_configs_whole(name):
     assert_close(timed, ref, cfg, odt, name + " timed step")
 
 
-@pytest.mark.parametrize("B", [1000, 6000])
-def test_large_batches_of_short_contexts(B):
+@pytest.mark.parametrize("cache,B", [("bf16", 1000), ("bf16", 6000), ("e4m3", 1000),
+                                     ("e4m3", 4000), ("e4m3tok", 1000), ("e4m3tok", 3000)])
+def test_large_batches_of_short_contexts(cache, B):
     """Thousands of short sequences (some empty): the per-sequence arrays push
     shared memory past two CTAs per SM (one wave becomes two) and the shares
-    hold hundreds of segments.  The timed one-kernel step, sampled rows
+    hold hundreds of segments.  The timed one-kernel step, every output row
     against the oracle, empty sequences exactly zero."""
-    cfg = wl.small_config(f"big_{B}", B, 32, 8, 128, "bf16", (0, 40), seed=31)
+    cfg = wl.small_config(f"big_{cache}_{B}", B, 32, 8, 128, cache, (0, 40), seed=31)
     w = wl.generate(cfg, device="cuda")
     run = DeviceRun(w)
     out = run.step_one_kernel("f32", overlap=True)
@@ -339,10 +340,4 @@ def test_large_batches_of_short_contexts(B):
     empty = np.nonzero(ctx == 0)[0]
     assert len(empty) > 0
     assert torch.count_nonzero(out[torch.as_tensor(empty, device="cuda")]) == 0
-    got = out.double().cpu().numpy()
-    rng = np.random.default_rng(B)
-    bs = rng.choice(np.nonzero(ctx > 0)[0], 24, replace=False)
-    pairs = [(int(b), int(rng.integers(cfg.q_heads))) for b in bs]
-    ref = oracle_rows(w, pairs)
-    assert_close(np.stack([got[b, hq] for b, hq in pairs]), np.stack([ref[p] for p in pairs]),
-                 cfg, "f32", f"batch {B}")
+    assert_close(out.double().cpu().numpy(), oracle_whole(w), cfg, "f32", f"{cache} batch {B}")
