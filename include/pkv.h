@@ -183,6 +183,10 @@ PKV_API size_t pkv_decode_workspace_bytes_multi(const pkv_cache_desc* desc, int3
  * Results are bitwise repeatable for the same inputs, sizes and device: the
  * work split depends only on the context lengths and the SM count, and
  * partial sums are always added in the same order.
+ * The kernel keeps five int32 per sequence in shared memory beside its page
+ * ring: batches past about 6000 sequences at head_dim 128 (6076 for 16-bit,
+ * 5979 for per-head and 7093 for per-token E4M3 caches) do not fit and
+ * return PKV_ERR_UNSUPPORTED.
  * The kernel is launched as a programmatic dependent of the preceding
  * kernel on the stream but waits for it to complete before reading any
  * input, so ordinary stream order holds. */
