@@ -315,6 +315,26 @@ def multi_query_decode(q, K, V, scale: float) -> np.ndarray:
                      for i in range(QL)])
 
 
+def chunk_attention(q, K, V, scale: float) -> np.ndarray:
+    """A chunk of QL new tokens of one sequence at once, for one query head
+    ([KVFA] opening section: the prefill processes the prompt in one parallel
+    pass; continuous-batching section: chunked prefill): q is [QL][d] for the
+    last QL positions of a sequence whose cached rows K, V are [n][d]
+    (n >= QL); row i sits at position n - QL + i and attends to rows
+    0 .. n - QL + i.  The rows of multi_query_decode, for the whole chunk
+    with library matrix products in fp64: scores S = scale q K^T, the
+    positions past each row's own masked out, then the two-pass softmax (row
+    maximum, exponentials, row sum) and the weighted sum of the V rows."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    n, QL = K.shape[0], q.shape[0]
+    assert n >= QL
+    S = scale * (q @ K.T)                                   # [QL][n]
+    last = n - QL + np.arange(QL)[:, None]                  # each row's position
+    S = np.where(np.arange(n)[None, :] <= last, S, -np.inf)
+    E = np.exp(S - S.max(axis=1, keepdims=True))
+    return (E @ V) / E.sum(axis=1, keepdims=True)
+
+
 def window_decode(q, K, V, scale: float, window: int, sinks: int) -> np.ndarray:
     """Multi-query decode under a sliding window with attention sinks ([AP]
     "Sparse attention: stop looking at everything": each token sees only the

@@ -69,3 +69,25 @@ def test_prefill_chunk_rows_match_library_sdpa():
                                              scale=scale)[0].numpy()
         got = oracle.multi_query_decode(Q, K, V, scale)
         assert np.allclose(got, ref, rtol=0, atol=1e-12), (n, QL, d)
+
+
+def test_chunk_attention_equals_the_row_definition():
+    """chunk_attention (library products over the whole chunk) against
+    multi_query_decode (each row the C definition) and against PyTorch's
+    scaled_dot_product_attention with the causal-at-the-end mask."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(15)
+    for n, QL, d in [(1, 1, 8), (300, 120, 64), (257, 257, 32), (513, 40, 16), (96, 5, 128)]:
+        Q = rng.standard_normal((QL, d)) * 2.0
+        K = rng.standard_normal((n, d))
+        V = rng.standard_normal((n, d))
+        scale = d ** -0.5
+        got = oracle.chunk_attention(Q, K, V, scale)
+        assert np.allclose(got, oracle.multi_query_decode(Q, K, V, scale), rtol=0, atol=1e-12)
+        pos = torch.arange(n - QL, n)[:, None]
+        mask = torch.arange(n)[None, :] <= pos
+        ref = F.scaled_dot_product_attention(torch.from_numpy(Q)[None], torch.from_numpy(K)[None],
+                                             torch.from_numpy(V)[None], attn_mask=mask[None],
+                                             scale=scale)[0].numpy()
+        assert np.allclose(got, ref, rtol=0, atol=1e-12), (n, QL, d)
