@@ -3,8 +3,10 @@
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
 (``paged_kv_cache_250_gb300``) never imports, links or calls it, and the two
-share no code: the oracle is plain C in fp64 (``pkv_oracle.c``) plus the thin
-numpy marshalling below.
+share no code: the oracle is plain C in fp64 (``pkv_oracle.c``), the thin
+numpy marshalling below, and a few numpy reference functions (library matrix
+products and table lookups in fp64) that restate definitions the C code also
+gives row by row.
 
 What it computes, and where each definition comes from, is stated beside each
 function in ``pkv_oracle.c``.  Every function here is pinned by the
